@@ -1,0 +1,12 @@
+"""GB300-native fused attention forward (sm_103a), exported through libattn's C ABI.
+
+The Python layer only marshals arguments: every step of the forward pass runs
+in the CUDA kernels of ``libattn.so``.  Importing this package does not load
+the library; the first call does, and it raises if the library is missing.
+"""
+from ._binding import (  # noqa: F401
+    ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT,
+    AttnError, attn_fwd, attn_fwd_ptr, attn_status_str, attn_check_device_status,
+    attn_kernel_launches, attn_debug_wait_timeout, library_path, load_library,
+    exported_symbols,
+)

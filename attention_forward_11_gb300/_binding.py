@@ -1,0 +1,141 @@
+"""ctypes binding for libattn.so -- argument marshalling only.
+
+The names mirror the C ABI in ``include/attn.h``.  Nothing here computes any
+part of the attention forward; if the shared library is missing the first call
+raises ``AttnError`` (there is no fallback).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_CUDA = 3
+ATTN_ERR_TIMEOUT = 4
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_NAME = "libattn.so"
+
+# Every symbol include/attn.h declares (checked by the CPU tests).
+EXPORTED = ("attn_fwd", "attn_status_str", "attn_check_device_status", "attn_kernel_launches",
+            "attn_debug_wait_timeout")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: status {status} ({_status_name(status)})")
+        self.status = status
+
+
+def _status_name(st: int) -> str:
+    return {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
+            3: "ATTN_ERR_CUDA", 4: "ATTN_ERR_TIMEOUT"}.get(st, "unknown")
+
+
+def library_path() -> str:
+    return os.environ.get("LIBATTN_PATH", os.path.join(_PKG, _LIB_NAME))
+
+
+def load_library():
+    """Load libattn.so (once); raises AttnError if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise AttnError(ATTN_ERR_CUDA, f"{path} is missing; run __graft_entry__.build()")
+        lib = ctypes.CDLL(path)
+        P = ctypes.c_void_p
+        I = ctypes.c_int
+        lib.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, ctypes.c_float, P]
+        lib.attn_fwd.restype = I
+        lib.attn_status_str.argtypes = [I]
+        lib.attn_status_str.restype = ctypes.c_char_p
+        lib.attn_check_device_status.argtypes = [P]
+        lib.attn_check_device_status.restype = I
+        lib.attn_kernel_launches.argtypes = []
+        lib.attn_kernel_launches.restype = ctypes.c_ulonglong
+        lib.attn_debug_wait_timeout.argtypes = [ctypes.c_uint, P]
+        lib.attn_debug_wait_timeout.restype = I
+        _lib = lib
+        return lib
+
+
+def exported_symbols():
+    lib = load_library()
+    return {name: getattr(lib, name, None) is not None for name in EXPORTED}
+
+
+def attn_status_str(status: int) -> str:
+    return load_library().attn_status_str(int(status)).decode()
+
+
+def _stream_handle(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def attn_fwd_ptr(q: int, k: int, v: int, o: int, lse: int, B: int, Sq: int, Skv: int, Hq: int,
+                 Hkv: int, D: int, causal: int, scale: float, stream: int) -> int:
+    """Raw-pointer call of the C entry point; returns the attn_status_t value."""
+    return int(load_library().attn_fwd(q, k, v, o, lse, B, Sq, Skv, Hq, Hkv, D, causal,
+                                       ctypes.c_float(scale), stream))
+
+
+def attn_fwd(q, k, v, o=None, lse=None, causal: int = 0, scale: float | None = None,
+             stream=None, want_lse: bool = True):
+    """O = softmax(scale * Q K^T [+ causal mask]) V and its fp32 log-sum-exp.
+
+    q: bf16 CUDA tensor [B, Sq, Hq, D]; k, v: [B, Skv, Hkv, D]; all contiguous.
+    o (optional): bf16 [B, Sq, Hq, D]; lse (optional): fp32 [B, Hq, Sq].
+    causal: 0 none, 1 bottom-right aligned.  Returns (o, lse or None).
+    Runs asynchronously on ``stream`` (default: torch's current stream).
+    """
+    import torch
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise AttnError(ATTN_ERR_INVALID_ARG, "q, k, v must be 4-d [B, S, H, D]")
+    B, Sq, Hq, D = q.shape
+    Skv, Hkv = k.shape[1], k.shape[2]
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise AttnError(ATTN_ERR_INVALID_ARG, f"{name} must be a contiguous bf16 CUDA tensor")
+    if tuple(v.shape) != tuple(k.shape) or k.shape[0] != B or k.shape[3] != D:
+        raise AttnError(ATTN_ERR_INVALID_ARG, "k/v shapes do not match q")
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    if scale is None:
+        scale = 1.0 / (D ** 0.5)
+    st = attn_fwd_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                      lse.data_ptr() if lse is not None else 0, B, Sq, Skv, Hq, Hkv, D,
+                      int(causal), float(scale), _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd")
+    return o, lse
+
+
+def attn_check_device_status(stream=None) -> int:
+    """Synchronise ``stream`` and return (then clear) the kernels' device status word."""
+    return int(load_library().attn_check_device_status(_stream_handle(stream)))
+
+
+def attn_kernel_launches() -> int:
+    """Number of kernels libattn has launched in this process."""
+    return int(load_library().attn_kernel_launches())
+
+
+def attn_debug_wait_timeout(poll_limit: int, stream=None) -> int:
+    """Launch the bounded-wait self-test kernel (an mbarrier nothing arrives on)."""
+    return int(load_library().attn_debug_wait_timeout(int(poll_limit), _stream_handle(stream)))

@@ -1,0 +1,193 @@
+"""fp64 CPU oracle for the attention forward pass -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+leg (and its ``--impl reference`` arm) may import this package.  The product
+path (the CUDA library and its Python binding) never imports it and shares no
+code with it.
+
+Contents
+  * ``attn_rows`` / ``attn_full`` -- the C oracle (``oracle.c``): textbook
+    two-pass softmax(scale * Q K^T [+ mask]) V in fp64, natural-log LSE.
+    Definition: the Pallas page (``attention_mgpu.py``), ``attention_reference``.
+  * ``partial_triple`` / ``merge_triples`` -- un-normalised (m, l, o) of a row
+    over a key range, and the merge rule of the kernbench page
+    (``_gqa_attention_prefill_short.py``, ``_merge_running``).
+  * ``round_bf16`` -- exact round-to-nearest-even of fp64 values to bf16, the
+    comparison value for the bf16 output.
+  * ``twin`` (module ``oracle.twin``) -- an independent numpy fp64 restatement
+    for tiny shapes, used to cross-check the C oracle by brute force.
+
+Parity pins (tests/test_oracle_pins.py) tie every function here to something
+other than itself: closed forms, library routines, invariants, brute force.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``oracle.c`` into ``liboracle.so`` with gcc + OpenMP (no -ffast-math)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    tmp = _LIB + ".tmp.%d" % os.getpid()
+    cmd = ["gcc", "-O2", "-fno-fast-math", "-fopenmp", "-shared", "-fPIC", "-std=c11",
+           _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def configure(lib):
+    """Declare the C signatures on a loaded oracle library."""
+    P = ctypes.c_void_p
+    L = ctypes.c_long
+    lib.oracle_attn_rows.argtypes = [P, P, P, L, L, L, L, L, L, ctypes.c_int,
+                                     ctypes.c_double, L, P, P, P]
+    lib.oracle_attn_rows.restype = ctypes.c_int
+    lib.oracle_attn_fwd.argtypes = [P, P, P, L, L, L, L, L, L, ctypes.c_int,
+                                    ctypes.c_double, P, P]
+    lib.oracle_attn_fwd.restype = ctypes.c_int
+    lib.oracle_partial_triple.argtypes = [P, P, P, L, L, L, L, L, L, ctypes.c_int,
+                                          ctypes.c_double, L, L, L, L, L, P, P, P]
+    lib.oracle_partial_triple.restype = ctypes.c_int
+    lib.oracle_num_threads.argtypes = []
+    lib.oracle_num_threads.restype = ctypes.c_int
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = configure(ctypes.CDLL(build()))
+    return _lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+def _check_inputs(q, k, v):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != np.uint16 or t.ndim != 4 or not t.flags.c_contiguous:
+            raise ValueError(f"{name} must be a C-contiguous 4-d uint16 array of bf16 bits")
+    B, Sq, Hq, D = q.shape
+    Bk, Skv, Hkv, Dk = k.shape
+    if v.shape != k.shape or Bk != B or Dk != D:
+        raise ValueError("k and v must be [B, Skv, Hkv, D] with q's B and D")
+    if Hq % Hkv:
+        raise ValueError("Hq must be a multiple of Hkv")
+    return B, Sq, Skv, Hq, Hkv, D
+
+
+def num_threads() -> int:
+    """OpenMP threads the C oracle uses."""
+    return int(_load().oracle_num_threads())
+
+
+def attn_rows(q, k, v, rows, causal: bool, scale: float):
+    """fp64 o (len(rows) x D) and lse (len(rows)) for the listed (b, h, i) rows."""
+    B, Sq, Skv, Hq, Hkv, D = _check_inputs(q, k, v)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
+    o = np.zeros((rows.shape[0], D), dtype=np.float64)
+    lse = np.zeros(rows.shape[0], dtype=np.float64)
+    rc = _load().oracle_attn_rows(_ptr(q), _ptr(k), _ptr(v), B, Sq, Skv, Hq, Hkv, D,
+                                  int(bool(causal)), float(scale), rows.shape[0],
+                                  _ptr(rows), _ptr(o), _ptr(lse))
+    if rc != 0:
+        raise ValueError("oracle_attn_rows rejected its arguments")
+    return o, lse
+
+
+def attn_full(q, k, v, causal: bool, scale: float):
+    """fp64 o [B,Sq,Hq,D] and lse [B,Hq,Sq] for every row."""
+    B, Sq, Skv, Hq, Hkv, D = _check_inputs(q, k, v)
+    o = np.zeros((B, Sq, Hq, D), dtype=np.float64)
+    lse = np.zeros((B, Hq, Sq), dtype=np.float64)
+    rc = _load().oracle_attn_fwd(_ptr(q), _ptr(k), _ptr(v), B, Sq, Skv, Hq, Hkv, D,
+                                 int(bool(causal)), float(scale), _ptr(o), _ptr(lse))
+    if rc != 0:
+        raise ValueError("oracle_attn_fwd rejected its arguments")
+    return o, lse
+
+
+def partial_triple(q, k, v, causal: bool, scale: float, b: int, h: int, i: int,
+                   j_lo: int, j_hi: int):
+    """Un-normalised (m, l, o) of row (b, h, i) over keys [j_lo, j_hi)."""
+    B, Sq, Skv, Hq, Hkv, D = _check_inputs(q, k, v)
+    m = np.zeros(1, dtype=np.float64)
+    l = np.zeros(1, dtype=np.float64)
+    o = np.zeros(D, dtype=np.float64)
+    rc = _load().oracle_partial_triple(_ptr(q), _ptr(k), _ptr(v), B, Sq, Skv, Hq, Hkv, D,
+                                       int(bool(causal)), float(scale), b, h, i, j_lo, j_hi,
+                                       _ptr(m), _ptr(l), _ptr(o))
+    if rc != 0:
+        raise ValueError("oracle_partial_triple rejected its arguments")
+    return float(m[0]), float(l[0]), o
+
+
+def merge_triples(t1, t2):
+    """Merge two un-normalised (m, l, o) triples over disjoint key sets.
+
+    The kernbench page's ``_merge_running``: m = max(m1, m2),
+    l = l1 e^(m1-m) + l2 e^(m2-m), o = o1 e^(m1-m) + o2 e^(m2-m).
+    An empty triple (m = -inf, l = 0) is the identity.
+    """
+    m1, l1, o1 = t1
+    m2, l2, o2 = t2
+    if m1 == -np.inf:
+        return m2, l2, np.array(o2, dtype=np.float64)
+    if m2 == -np.inf:
+        return m1, l1, np.array(o1, dtype=np.float64)
+    m = max(m1, m2)
+    a1 = np.exp(m1 - m)
+    a2 = np.exp(m2 - m)
+    return m, l1 * a1 + l2 * a2, np.asarray(o1) * a1 + np.asarray(o2) * a2
+
+
+def finish_triple(t):
+    """(normalised o, lse) of a merged triple; o = 0, lse = -inf when nothing is visible."""
+    m, l, o = t
+    if l <= 0.0:
+        return np.zeros_like(np.asarray(o, dtype=np.float64)), -np.inf
+    return np.asarray(o) / l, m + np.log(l)
+
+
+def round_bf16(x) -> np.ndarray:
+    """Exact round-to-nearest-even of fp64 values to bf16 (returned as fp64).
+
+    bf16 keeps 8 significant bits and fp32's exponent range.  The value is
+    split as x = f * 2^e with 0.5 <= |f| < 1; f * 2^8 is rounded half-to-even;
+    below the smallest normal (2^-126) the grid is fixed at 2^-133.
+    Overflow past bf16's largest finite value goes to +-inf.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    out = np.array(x, dtype=np.float64, copy=True)
+    finite = np.isfinite(x) & (x != 0.0)
+    xf = x[finite]
+    f, e = np.frexp(xf)
+    normal = e >= -125  # |x| >= 2^-126  <=>  e - 1 >= -126
+    r = np.empty_like(xf)
+    r[normal] = np.ldexp(np.rint(np.ldexp(f[normal], 8)), e[normal] - 8)
+    r[~normal] = np.ldexp(np.rint(np.ldexp(xf[~normal], 133)), -133)
+    max_bf16 = float.fromhex("0x1.fep127")
+    r[np.abs(r) > max_bf16] = np.copysign(np.inf, r[np.abs(r) > max_bf16])
+    out[finite] = r
+    return out
+
+
+def bf16_bits_to_f64(bits) -> np.ndarray:
+    """Widen bf16 bit patterns (uint16) to fp64 exactly."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)

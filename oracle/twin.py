@@ -1,0 +1,47 @@
+"""Independent numpy fp64 restatement of attention, for tiny shapes only.
+
+TEST INFRASTRUCTURE: it exists to cross-check the C oracle by brute force and
+shares no code with it.  Written per head with a dense masked logit matrix
+(one numpy matmul per head), a masked row maximum, exponentials, row sums and
+a second matmul with V -- the Pallas page's ``attention_reference`` (fp32
+einsum, ``logits.max``, ``exp``, divide by the row sum) in fp64 with the
+caller's scale, a bottom-right causal mask and a natural-log LSE.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def _widen(bits):
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(
+        np.float64)
+
+
+def attention(q_bits, k_bits, v_bits, causal: bool, scale: float):
+    """Returns (o [B,Sq,Hq,D] fp64, lse [B,Hq,Sq] fp64)."""
+    q, k, v = _widen(q_bits), _widen(k_bits), _widen(v_bits)
+    B, Sq, Hq, D = q.shape
+    Skv, Hkv = k.shape[1], k.shape[2]
+    group = Hq // Hkv
+    o = np.zeros((B, Sq, Hq, D))
+    lse = np.zeros((B, Hq, Sq))
+    qi = np.arange(Sq)[:, None]
+    kj = np.arange(Skv)[None, :]
+    visible = (kj <= qi + (Skv - Sq)) if causal else np.ones((Sq, Skv), dtype=bool)
+    for b in range(B):
+        for h in range(Hq):
+            g = h // group
+            logits = scale * (q[b, :, h, :] @ k[b, :, g, :].T)
+            logits = np.where(visible, logits, -np.inf)
+            for i in range(Sq):
+                row = logits[i]
+                if not np.any(visible[i]):
+                    o[b, i, h, :] = 0.0
+                    lse[b, h, i] = -np.inf
+                    continue
+                m = row[visible[i]].max()
+                w = np.where(visible[i], np.exp(row - m), 0.0)
+                l = w.sum()
+                o[b, i, h, :] = (w @ v[b, :, g, :]) / l
+                lse[b, h, i] = m + np.log(l)
+    return o, lse

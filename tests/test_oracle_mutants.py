@@ -1,0 +1,93 @@
+"""The pins must be able to fail: plant plausible mistakes in a copy of the
+oracle's C source (on the CPU), rebuild it, and check that the pin suite
+rejects every mutant."""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+import oracle
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(os.path.dirname(HERE), "oracle", "oracle.c")
+
+# (name, text in oracle.c, replacement)
+MUTANTS = [
+    ("drop_scale", "double s = p->scale * acc;", "double s = acc;"),
+    ("gqa_modulo", "const long g = h / (p->Hq / p->Hkv);", "const long g = h % p->Hkv;"),
+    ("mask_off_by_one", "long end = i + (p->Skv - p->Sq) + 1;", "long end = i + (p->Skv - p->Sq);"),
+    ("top_left_mask", "long end = i + (p->Skv - p->Sq) + 1;", "long end = i + 1;"),
+    ("base2_lse", "= m + log(l);", "= m + log2(l);"),
+    ("no_normalise", "for (long d = 0; d < D; ++d) o[d] /= l;", ";"),
+    ("exp2_weights", "double w = exp(s_buf[j - j_lo] - m);", "double w = exp2(s_buf[j - j_lo] - m);"),
+    ("no_max_shift", "double w = exp(s_buf[j - j_lo] - m);", "double w = exp(s_buf[j - j_lo]);"),
+    ("k_by_query_row", "const uint16_t *krow = p->k + ((b * p->Skv + j) * p->Hkv + g) * D;",
+     "const uint16_t *krow = p->k + ((b * p->Skv + (i < p->Skv ? i : j)) * p->Hkv + g) * D;"),
+    ("k_head_modulo", "const uint16_t *krow = p->k + ((b * p->Skv + j) * p->Hkv + g) * D;",
+     "const uint16_t *krow = p->k + ((b * p->Skv + j) * p->Hkv + h % p->Hkv) * D;"),
+    ("v_by_query_row", "const uint16_t *vrow = p->v + ((b * p->Skv + j) * p->Hkv + g) * D;",
+     "const uint16_t *vrow = p->v + ((b * p->Skv + (i < p->Skv ? i : j)) * p->Hkv + g) * D;"),
+    ("sign_flip", "double s = p->scale * acc;", "double s = -p->scale * acc;"),
+]
+
+PIN_TESTS = [
+    "test_hand_worked_two_keys", "test_zero_query_closed_form", "test_constant_v_rows",
+    "test_causal_row0_is_v0", "test_one_hot_limit_pins_operand_roles", "test_matches_scipy_softmax",
+    "test_brute_force_twin", "test_gqa_head_repeat_equivalence",
+    "test_bottom_right_equals_tail_of_square_causal", "test_shift_invariance_large_logits",
+    "test_merge_identity_random_chunks",
+]
+
+
+def _build_mutant(tmp_path, name, old, new):
+    text = open(SRC).read()
+    assert text.count(old) >= 1, f"mutation anchor for {name} not found"
+    src = tmp_path / f"{name}.c"
+    src.write_text(text.replace(old, new))
+    so = tmp_path / f"lib{name}.so"
+    subprocess.run(["gcc", "-O1", "-fopenmp", "-shared", "-fPIC", "-std=c11", str(src), "-o",
+                    str(so), "-lm"], check=True)
+    return oracle.configure(ctypes.CDLL(str(so)))
+
+
+def _run_pins(monkeypatch, lib):
+    import test_oracle_pins as pins
+    monkeypatch.setattr(oracle, "_lib", lib)
+    failures = 0
+    for name in PIN_TESTS:
+        fn = getattr(pins, name)
+        params = getattr(fn, "pytestmark", [])
+        cases = [dict()]
+        for mark in params:
+            if mark.name == "parametrize":
+                argnames = [a.strip() for a in mark.args[0].split(",")] if isinstance(
+                    mark.args[0], str) else list(mark.args[0])
+                new_cases = []
+                for c in cases:
+                    for val in mark.args[1]:
+                        vals = val if len(argnames) > 1 else (val,)
+                        new_cases.append({**c, **dict(zip(argnames, vals))})
+                cases = new_cases
+        for kw in cases:
+            try:
+                fn(**kw)
+            except (AssertionError, ValueError, FloatingPointError):
+                failures += 1
+    return failures
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_reject_planted_mistake(tmp_path, monkeypatch, name, old, new):
+    import sys
+    sys.path.insert(0, HERE)
+    lib = _build_mutant(tmp_path, name, old, new)
+    assert _run_pins(monkeypatch, lib) > 0, f"mutant {name} passed every pin"
+
+
+def test_unmutated_copy_passes(tmp_path, monkeypatch):
+    import sys
+    sys.path.insert(0, HERE)
+    lib = _build_mutant(tmp_path, "identity", "int oracle_num_threads(void)",
+                        "int oracle_num_threads(void)")
+    assert _run_pins(monkeypatch, lib) == 0
