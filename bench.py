@@ -1,0 +1,393 @@
+"""Benchmark of the GB300 attention forward (one step = one forward pass).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints one JSON line.  `value` is TFLOP/s with the causal FLOP count halved
+(4*B*Hq*Sq*Skv*D, integer-halved when causal -- the count the Pallas page's
+benchmark `main` uses), from CUDA events around each kernel launch on its
+stream, inputs resident in HBM, L2 flushed (a 256 MiB write) between steps.
+`e2e` is the same metric through the C ABI with pinned host buffers: the
+host->device copies of Q, K, V and the device->host copies of O and LSE are
+inside its timed region.  `roofline` relates the kernel to the measured dense
+bf16 tensor peak.  `cpu_baseline` times the fp64 oracle on a bounded sample of
+the same workload on the host cores.
+
+Under torchrun (N > 1) every rank runs an independent replica of the workload
+on its own GPU (the forward pass has no exchange step); the max over ranks of
+the timed region divides the work of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s (bf16, causal FLOPs halved) and % of GB300 dense bf16 peak"
+UNIT = "TFLOP/s"
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def metric_flops(w) -> int:
+    f = 4 * w.B * w.Hq * w.Sq * w.Skv * w.D
+    return f // 2 if w.causal else f
+
+
+def visible_pairs(w) -> int:
+    """Exact number of (query row, key) pairs the mask lets through, per head and batch."""
+    if not w.causal:
+        return w.Sq * w.Skv
+    off = w.Skv - w.Sq
+    total = 0
+    for i in range(w.Sq):
+        total += max(0, min(w.Skv, i + off + 1))
+    return total
+
+
+def exact_flops(w) -> int:
+    return 4 * w.D * w.B * w.Hq * visible_pairs(w)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "attention_forward_11_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        rec = d.get(workload)
+        if rec and rec.get("kernel_source_digest") == kernel_source_digest():
+            return rec["dram_bytes_per_launch"]
+    except Exception:
+        pass
+    return None
+
+
+# ------------------------------------------------------------------ clocks (NVML, read-only)
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML while running."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x2: "applications_clocks_setting", 0x1: "gpu_idle"}
+
+    def __init__(self, index: int, period_s: float = 0.005):
+        self.samples, self.reasons, self.max_mhz = [], set(), None
+        self.period = period_s
+        self._stop = threading.Event()
+        self._thread = None
+        try:
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            self.handle = ctypes.c_void_p()
+            if self.nvml.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(self.handle)) != 0:
+                raise OSError("no handle")
+            mx = ctypes.c_uint()
+            if self.nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+        except OSError:
+            self.nvml = None
+
+    def _run(self):
+        mhz = ctypes.c_uint()
+        reasons = ctypes.c_ulonglong()
+        get_reasons = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self._stop.is_set():
+            if self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(mhz)) == 0:
+                self.samples.append(mhz.value)
+            if get_reasons(self.handle, ctypes.byref(reasons)) == 0:
+                for bit, name in self.REASONS.items():
+                    if reasons.value & bit and bit != 0x1:
+                        self.reasons.add(name)
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.nvml is not None:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join()
+
+    def summary(self):
+        if self.nvml is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "NVML unavailable"}
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                "samples": len(self.samples)}
+
+
+# ------------------------------------------------------------------ CPU baseline (oracle)
+def oracle_sample_rate(w, target_s: float, seed: int = 0, q=None, k=None, v=None):
+    """Times the fp64 oracle on a sample of the workload's query rows sized to
+    about `target_s` seconds; returns (TFLOP/s, seconds, rows, threads)."""
+    import numpy as np
+    import oracle
+    from attention_forward_11_gb300 import inputs
+    if q is None:
+        q, k, v = inputs.make_workload(w, seed=seed)
+    rng = np.random.default_rng(seed + 17)
+
+    def rows_of(n):
+        return np.stack([rng.integers(0, w.B, n), rng.integers(0, w.Hq, n),
+                         rng.integers(0, w.Sq, n)], axis=1).astype(np.int64)
+
+    def flops_of(rows):
+        off = w.Skv - w.Sq
+        vis = np.minimum(w.Skv, rows[:, 2] + off + 1) if w.causal else np.full(len(rows), w.Skv)
+        return float(4 * w.D * np.maximum(vis, 0).sum())
+
+    probe = rows_of(32)
+    t0 = time.perf_counter()
+    oracle.attn_rows(q, k, v, probe, bool(w.causal), w.scale)
+    dt = max(time.perf_counter() - t0, 1e-4)
+    n = int(max(32, min(2_000_000, 32 * target_s / dt)))
+    rows = rows_of(n)
+    t0 = time.perf_counter()
+    oracle.attn_rows(q, k, v, rows, bool(w.causal), w.scale)
+    dt = time.perf_counter() - t0
+    return flops_of(rows) / dt / 1e12, dt, n, oracle.num_threads()
+
+
+# ------------------------------------------------------------------ main arms
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args, w):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from attention_forward_11_gb300 import inputs
+    oracle.build()
+    q, k, v = inputs.make_workload(w, seed=0)
+    per_step = args.ref_step_seconds
+    vals, secs, rows = [], [], 0
+    for i in range(args.warmup + args.steps):
+        tf, dt, n, cores = oracle_sample_rate(w, per_step, seed=i, q=q, k=k, v=v)
+        if i >= args.warmup:
+            vals.append(tf)
+            secs.append(dt)
+            rows = n
+    value = statistics.mean(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * metric_flops(w) / (value * 1e12),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {**w.as_dict(), "parallelism": "replicas"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{rows} random query rows of the workload per step, "
+                                   f"~{per_step:.0f} s each; ms_per_step extrapolated to the "
+                                   f"whole workload"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    del np
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w):
+    import numpy as np
+    import torch
+
+    import attention_forward_11_gb300 as fa
+    from attention_forward_11_gb300 import build as libbuild
+    from attention_forward_11_gb300 import inputs
+
+    world, rank, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        libbuild.build()
+    if world > 1:
+        dist.barrier()
+    fa.load_library()
+
+    q_h, k_h, v_h = inputs.make_workload(w, seed=rank)
+
+    def pinned(bits):
+        t = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+        return t.pin_memory()
+
+    qp, kp, vp = pinned(q_h), pinned(k_h), pinned(v_h)
+    q = qp.to(dev)
+    k = kp.to(dev)
+    v = vp.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
+    o_h = torch.empty(o.shape, dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+
+    def step():
+        st = fa.attn_fwd_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                             lse.data_ptr(), w.B, w.Sq, w.Skv, w.Hq, w.Hkv, w.D, w.causal,
+                             w.scale, sh)
+        if st != fa.ATTN_OK:
+            raise fa.AttnError(st, "attn_fwd")
+
+    # ---- warm-up
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    if fa.attn_check_device_status(stream) != fa.ATTN_OK:
+        raise RuntimeError("device status not OK after warm-up")
+
+    # ---- timed: K steps, L2 flushed between steps, events around each launch
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = fa.attn_kernel_launches()
+    with ClockSampler(local) as clocks:
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall
+    launches = fa.attn_kernel_launches() - launches0
+    if world > 1:
+        dist.barrier()
+    if fa.attn_check_device_status(stream) != fa.ATTN_OK:
+        raise RuntimeError("device status not OK after the timed region")
+    times_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    kernel_s = sum(times_ms) / 1e3
+
+    # ---- e2e: pinned host buffers, copies inside the timed region
+    e2e_steps = max(3, min(args.steps, 20))
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    for i in range(e2e_steps + 1):
+        if i == 1:
+            torch.cuda.synchronize(dev)
+            e_start.record(stream)
+        q.copy_(qp, non_blocking=True)
+        k.copy_(kp, non_blocking=True)
+        v.copy_(vp, non_blocking=True)
+        step()
+        o_h.copy_(o, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+    e_end.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_s = e_start.elapsed_time(e_end) / 1e3
+
+    if world > 1:
+        t = torch.tensor([kernel_s, e2e_s], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        kernel_s, e2e_s = float(t[0]), float(t[1])
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+
+    flops = metric_flops(w)
+    value = world * flops * args.steps / kernel_s / 1e12
+    e2e_value = world * flops * e2e_steps / e2e_s / 1e12
+    peak, peak_kind = load_peaks()
+    exact = exact_flops(w)
+    mean_launch_s = kernel_s / args.steps
+    achieved = exact / mean_launch_s / 1e12
+    bytes_in = q.numel() * 2 + k.numel() * 2 + v.numel() * 2
+    bytes_out = o.numel() * 2 + lse.numel() * 4
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * mean_launch_s, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {**w.as_dict(), "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "flushed between steps (256 MiB write); inputs also exceed L2",
+                   "metric_flops_per_step": flops, "exact_visible_pair_flops_per_step": exact,
+                   "pct_of_peak": 100.0 * value / peak},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": load_traffic(w.name),
+                     "peak_source": f"bf16_tflops (burst) of {peak_kind}",
+                     "kernel": "attn::fmha_fwd_kernel",
+                     "algorithmic_unit": "4*D FLOPs per visible (q-row, key, q-head)"},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": bytes_in,
+                "d2h_bytes_per_step": bytes_out, "steps": e2e_steps},
+        "gpu_launches": int(launches),
+        "clocks": clocks.summary(),
+        "wall_s_timed_region": t_wall,
+        "kernel_ms": {"min": min(times_ms), "median": statistics.median(times_ms),
+                      "max": max(times_ms)},
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        tf, dt, n, cores = oracle_sample_rate(w, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": f"{n} random query rows of {w.name} "
+                                          f"({dt:.1f} s of fp64 oracle work)"}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    from attention_forward_11_gb300 import inputs
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=inputs.HEADLINE, choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=3.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
+    w = inputs.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

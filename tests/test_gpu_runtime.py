@@ -1,0 +1,54 @@
+"""GPU checks of the runtime around the kernel: launch accounting, argument
+errors on real tensors, and the bounded-wait failure path (no GPU fault: the
+self-test kernel waits on an mbarrier nothing arrives on, gives up after a
+bounded number of polls and reports ATTN_ERR_TIMEOUT; the context stays usable)."""
+import math
+
+import pytest
+
+import attention_forward_11_gb300 as fa
+from attention_forward_11_gb300 import inputs
+from parity import check_full, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def test_timeout_is_reported_and_cleared():
+    assert fa.attn_check_device_status() == fa.ATTN_OK
+    assert fa.attn_debug_wait_timeout(1000) == fa.ATTN_OK
+    assert fa.attn_check_device_status() == fa.ATTN_ERR_TIMEOUT
+    assert fa.attn_check_device_status() == fa.ATTN_OK
+    # the context is still usable afterwards
+    q, k, v = inputs.make_qkv(1, 256, 256, 2, 2, 128, seed=1)
+    check_full(q, k, v, 1, 1 / math.sqrt(128), "after timeout self-test")
+
+
+def test_one_launch_per_call():
+    import torch
+    q, k, v = inputs.make_qkv(1, 256, 256, 2, 2, 128, seed=1)
+    dq, dk, dv = to_device(q), to_device(k), to_device(v)
+    before = fa.attn_kernel_launches()
+    for _ in range(3):
+        fa.attn_fwd(dq, dk, dv, causal=1)
+    torch.cuda.synchronize()
+    assert fa.attn_kernel_launches() - before == 3
+
+
+def test_bad_tensors_raise_without_launch():
+    import torch
+    q = torch.zeros(1, 64, 2, 128, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(1, 64, 2, 128, dtype=torch.bfloat16, device="cuda")
+    before = fa.attn_kernel_launches()
+    with pytest.raises(fa.AttnError):
+        fa.attn_fwd(q.float(), k, k)                     # wrong dtype
+    with pytest.raises(fa.AttnError):
+        fa.attn_fwd(q, k[:, :, :1].contiguous(), k)      # k/v shape mismatch
+    with pytest.raises(fa.AttnError) as e:
+        fa.attn_fwd(q[..., :64].contiguous(), k[..., :64].contiguous(), k[..., :64].contiguous())
+    assert e.value.status == fa.ATTN_ERR_UNSUPPORTED
+    with pytest.raises(fa.AttnError) as e:
+        flat = torch.zeros(64 * 2 * 128 + 8, dtype=torch.bfloat16, device="cuda")
+        mis = flat[1:1 + 64 * 2 * 128].view(1, 64, 2, 128)   # 2-byte offset: not 16-byte aligned
+        fa.attn_fwd(mis, k, k)
+    assert e.value.status == fa.ATTN_ERR_INVALID_ARG
+    assert fa.attn_kernel_launches() == before

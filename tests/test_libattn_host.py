@@ -1,0 +1,94 @@
+"""CPU-only checks of the C ABI: the library loads, exports every symbol the
+header declares, and its host-side validation rejects bad requests before any
+CUDA call (no GPU is touched: every call here returns before launching)."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+import attention_forward_11_gb300 as fa
+from attention_forward_11_gb300 import build as fa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fa_build.build()
+    return fa.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_expected_entry_points():
+    assert declared_functions() == sorted(fa._binding.EXPORTED)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    assert fa.attn_status_str(0) == "ATTN_OK"
+    assert fa.attn_status_str(1) == "ATTN_ERR_INVALID_ARG"
+    assert fa.attn_status_str(2) == "ATTN_ERR_UNSUPPORTED"
+    assert fa.attn_status_str(3) == "ATTN_ERR_CUDA"
+    assert fa.attn_status_str(4) == "ATTN_ERR_TIMEOUT"
+    assert fa.attn_status_str(99) == "ATTN_UNKNOWN_STATUS"
+
+
+# fake, 16-byte aligned, non-overlapping addresses: validation never dereferences them
+Q, K, V, O, L = 0x1000000, 0x2000000, 0x3000000, 0x4000000, 0x5000000
+GOOD = dict(q=Q, k=K, v=V, o=O, lse=L, B=1, Sq=256, Skv=256, Hq=2, Hkv=2, D=128, causal=1,
+            scale=0.088, stream=0)
+
+
+def call(**over):
+    a = {**GOOD, **over}
+    return fa.attn_fwd_ptr(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Sq"], a["Skv"],
+                           a["Hq"], a["Hkv"], a["D"], a["causal"], a["scale"], a["stream"])
+
+
+@pytest.mark.parametrize("over", [
+    dict(q=0), dict(k=0), dict(v=0), dict(o=0),
+    dict(B=0), dict(Sq=0), dict(Skv=-1), dict(Hq=0), dict(Hkv=0), dict(D=0),
+    dict(Hq=6, Hkv=4), dict(causal=2), dict(causal=-1),
+    dict(scale=0.0), dict(scale=-1.0), dict(scale=math.nan), dict(scale=math.inf),
+    dict(q=Q + 8), dict(k=K + 2), dict(v=V + 4), dict(o=O + 1), dict(lse=L + 2),
+    dict(o=Q + 64), dict(o=K), dict(lse=O + 16),
+], ids=lambda d: ",".join(f"{k}={v}" for k, v in d.items()))
+def test_invalid_arguments_rejected(lib, over):
+    assert call(**over) == fa.ATTN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("D", [64, 256, 96])
+def test_other_head_dims_unsupported(lib, D):
+    assert call(D=D) == fa.ATTN_ERR_UNSUPPORTED
+
+
+def test_wait_selftest_rejects_bad_limit(lib):
+    assert fa._binding.attn_debug_wait_timeout(0, 0) == fa.ATTN_ERR_INVALID_ARG
+    assert fa._binding.attn_debug_wait_timeout((1 << 20) + 1, 0) == fa.ATTN_ERR_INVALID_ARG
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(fa._binding, "_lib", None)
+    monkeypatch.setenv("LIBATTN_PATH", str(tmp_path / "nope.so"))
+    with pytest.raises(fa.AttnError):
+        fa.load_library()
+    monkeypatch.setattr(fa._binding, "_lib", None)
+
+
+def test_library_does_not_link_the_oracle(lib):
+    # the product library and the oracle share no code: no oracle symbol in libattn
+    for name in ("oracle_attn_rows", "oracle_attn_fwd", "oracle_partial_triple"):
+        assert not hasattr(lib, name)
+    assert ctypes.CDLL(fa.library_path()) is not None
