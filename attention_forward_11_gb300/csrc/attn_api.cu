@@ -57,16 +57,21 @@ bool encode_bshd(CUtensorMap* map, const void* ptr, int B, int S, int H, int D) 
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool ensure_kernel_attrs(int dev) {
+// Per-device one-time set-up: the kernel's shared-memory opt-in and the SM count.
+bool device_setup(int dev, int* sm_count) {
     static std::mutex mu;
-    static bool done[kMaxDevices] = {};
+    static int sms[kMaxDevices] = {};
     if (dev < 0 || dev >= kMaxDevices) return false;
     std::lock_guard<std::mutex> lock(mu);
-    if (done[dev]) return true;
-    if (cudaFuncSetAttribute(attn::fmha_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             attn::kSmemBytes) != cudaSuccess)
-        return false;
-    done[dev] = true;
+    if (sms[dev] == 0) {
+        int n = 0;
+        if (cudaFuncSetAttribute(attn::fmha_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 attn::kSmemBytes) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+            return false;
+        sms[dev] = n;
+    }
+    *sm_count = sms[dev];
     return true;
 }
 
@@ -119,18 +124,22 @@ extern "C" attn_status_t attn_fwd(const void* q, const void* k, const void* v, v
         p.n_head_units = Hq;
         p.n_row_units = (Sq + attn::kTiles * attn::kBM - 1) / (attn::kTiles * attn::kBM);
     }
-    const long long grid = (long long)p.n_row_units * B * p.n_head_units;
-    if (grid > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+    const long long n_units = (long long)p.n_row_units * B * p.n_head_units;
+    if (n_units > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+    p.n_units = static_cast<int>(n_units);
+    p.o = static_cast<uint16_t*>(o);
 
-    CUtensorMap tm_q, tm_k, tm_v, tm_o;
+    CUtensorMap tm_q, tm_k, tm_v;
     if (!encode_bshd(&tm_q, q, B, Sq, Hq, D) || !encode_bshd(&tm_k, k, B, Skv, Hkv, D) ||
-        !encode_bshd(&tm_v, v, B, Skv, Hkv, D) || !encode_bshd(&tm_o, o, B, Sq, Hq, D))
+        !encode_bshd(&tm_v, v, B, Skv, Hkv, D))
         return ATTN_ERR_CUDA;
 
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || !ensure_kernel_attrs(dev)) return ATTN_ERR_CUDA;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || !device_setup(dev, &sms)) return ATTN_ERR_CUDA;
+    // persistent grid: at most one CTA per SM (the CTA holds all 512 TMEM columns)
+    const int grid = static_cast<int>(n_units < sms ? n_units : sms);
     attn::fmha_fwd_kernel<<<static_cast<unsigned int>(grid), attn::kThreads, attn::kSmemBytes,
-                            stream>>>(tm_q, tm_k, tm_v, tm_o, p);
+                            stream>>>(tm_q, tm_k, tm_v, p);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return ATTN_OK;

@@ -1,15 +1,20 @@
 // fmha_fwd_sm103.cuh -- fused attention forward for sm_103a (GB300).
 //
-// One CTA owns two 128-row query tiles that read the same K/V head: either two
+// Work unit = two 128-row query tiles that read the same K/V head: either two
 // consecutive row tiles of one query head, or (when the GQA group has an even
 // number of query heads) the same rows of two query heads of one group, so
-// every K/V tile brought into shared memory feeds 256 query rows.
+// every K/V tile brought into shared memory feeds 256 query rows.  Units are
+// numbered longest first (causal row tiles near the end of the sequence visit
+// the most KV tiles -- the Choreo tutorial's non-persistent schedule); a
+// persistent grid of at most one CTA per SM takes them in a snake order
+// (round r: CTA c takes unit r*G + c, or r*G + G-1-c on odd rounds), so the
+// next unit's Q is loaded while the current one finishes.
 //
 // Warp roles (320 threads):
 //   warps 0-3  softmax warpgroup of tile 0 (one query row per thread)
 //   warps 4-7  softmax warpgroup of tile 1
-//   warp  8    MMA issuer (one thread): S_t = Q_t K^T and O_t += P_t V on tcgen05
-//   warp  9    TMA producer (one thread): Q once, then K and V tiles through
+//   warp  8    MMA issuer (one elected lane): S_t = Q_t K^T and O_t += P_t V on tcgen05
+//   warp  9    TMA producer (one thread): Q of each unit, K and V tiles through
 //              two shared-memory rings guarded by full/empty mbarriers
 //
 // Tensor memory (512 columns x 128 lanes, fp32): S_0 | S_1 | O_0 | O_1, 128 columns
@@ -20,16 +25,19 @@
 // maximum is kept in log2 units of the scaled logits so that each weight is one
 // FMA and one ex2 (scale * log2e folded into the FMA), the running sum is
 // rescaled by alpha = 2^(m_old - m_new), and O is divided by the sum once at the
-// end.  The maximum used for the exponentials is only raised when the tile
-// maximum exceeds it by more than 2^8; otherwise the stale maximum is kept
-// (weights stay <= 256, exact in the same arithmetic since l and O share it),
-// so O in tensor memory is rescaled only on the rare tiles that raise it.
+// end.  The maximum used for the exponentials is only raised when a tile's
+// maximum exceeds it by more than 8 (log2 units); otherwise the stale maximum
+// is kept (weights stay <= 256; l and O share it, so the quotient is the same),
+// and O in tensor memory is rescaled only on the rare tiles that raise it.
+// (Optionally, ATTN_SPECULATIVE_EXP, the weights are computed against the stale
+// maximum while the tile maximum is still being reduced, and only rows whose
+// maximum rises recompute them; that keeps every logit live and needs more
+// registers per thread than this 10-warp layout leaves.)
 //
 // Causal (bottom-right aligned: key j visible from row i iff j <= i + Skv - Sq):
 // KV tiles entirely above a tile's last visible key are never loaded or
 // multiplied; the element mask is applied only on the tiles that cross the
-// diagonal or the ragged key tail.  Row tiles are launched longest first (the
-// Choreo tutorial's non-persistent schedule) so the short tiles fill the tail.
+// diagonal or the ragged key tail.
 //
 // Every mbarrier wait is bounded: when a wait runs out, the thread records
 // ATTN_ERR_TIMEOUT in the device status word and raises a CTA abort flag; all
@@ -41,14 +49,24 @@
 
 #include "sm103_ptx.cuh"
 
+#ifndef ATTN_KSTAGES
+#define ATTN_KSTAGES 2
+#endif
+#ifndef ATTN_VSTAGES
+#define ATTN_VSTAGES 3
+#endif
+#ifndef ATTN_SPECULATIVE_EXP
+#define ATTN_SPECULATIVE_EXP 0  // weights against the stale max before the tile max is known
+#endif
+
 namespace attn {
 
 constexpr int kBM = 128;                 // query rows per tile (= TMEM lanes)
 constexpr int kBN = 128;                 // keys per KV tile
 constexpr int kHeadDim = 128;            // D
-constexpr int kTiles = 2;                // query tiles per CTA
-constexpr int kKStages = 2;              // K ring depth
-constexpr int kVStages = 2;              // V ring depth
+constexpr int kTiles = 2;                // query tiles per unit
+constexpr int kKStages = ATTN_KSTAGES;   // K ring depth
+constexpr int kVStages = ATTN_VSTAGES;   // V ring depth
 constexpr int kTileBytes = kBM * kHeadDim * 2;   // 32 KB bf16 tile (Q, K or V)
 constexpr int kHalfBytes = kTileBytes / 2;       // one 64-column, 128-byte-swizzled half
 constexpr int kSoftmaxWarps = 4 * kTiles;
@@ -66,15 +84,17 @@ constexpr int kSmemK = kSmemQ + kTiles * kTileBytes;
 constexpr int kSmemV = kSmemK + kKStages * kTileBytes;
 constexpr int kSmemBar = kSmemV + kVStages * kTileBytes;
 enum : int {
-    BAR_Q = 0,
-    BAR_KFULL = 1,
+    BAR_QFULL = 0,
+    BAR_QEMPTY = BAR_QFULL + kTiles,
+    BAR_KFULL = BAR_QEMPTY + kTiles,
     BAR_KEMPTY = BAR_KFULL + kKStages,
     BAR_VFULL = BAR_KEMPTY + kKStages,
     BAR_VEMPTY = BAR_VFULL + kVStages,
     BAR_SFULL = BAR_VEMPTY + kVStages,
     BAR_PFULL = BAR_SFULL + kTiles,
     BAR_ODONE = BAR_PFULL + kTiles,
-    BAR_MMADONE = BAR_ODONE + kTiles,
+    BAR_OFREE = BAR_ODONE + kTiles,
+    BAR_MMADONE = BAR_OFREE + kTiles,
     BAR_COUNT
 };
 constexpr int kSmemTmemSlot = kSmemBar + BAR_COUNT * 8;
@@ -92,10 +112,12 @@ struct FwdParams {
     int B, Sq, Skv, Hq, Hkv;
     int causal;             // 0 or 1 (bottom-right)
     float scale_log2;       // softmax scale * log2(e)
+    uint16_t* o;            // [B, Sq, Hq, D] bf16
     float* lse;             // [B, Hq, Sq] fp32, or nullptr
-    int head_pairs;         // 1: the CTA's tiles are two heads of a GQA group, same rows
+    int head_pairs;         // 1: a unit's tiles are two heads of a GQA group, same rows
     int n_row_units;        // row units per (batch, head unit)
     int n_head_units;       // head units per batch
+    int n_units;            // n_row_units * B * n_head_units
     unsigned int poll_limit;  // bound on every mbarrier poll loop
 };
 
@@ -105,7 +127,7 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
                                              unsigned int limit) {
     for (unsigned int i = 0; i < limit; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
+        if ((i & 15u) == 15u && *abort_flag) return false;
     }
     *abort_flag = 1;
     atomicOr(&g_attn_status, kStatusTimeout);
@@ -146,10 +168,52 @@ __device__ __forceinline__ int kv_tiles_for(const FwdParams& p, int row0) {
     return n < n_all ? (int)n : n_all;
 }
 
+// Decoded work unit.
+struct Unit {
+    int b, hkv;
+    int hq0, hq1;      // query heads of tile 0 / tile 1
+    int row0, row1;    // first query row of tile 0 / tile 1
+    int n0, n1;        // KV tiles each tile visits
+    __device__ __forceinline__ int hq(int t) const { return t ? hq1 : hq0; }
+    __device__ __forceinline__ int row(int t) const { return t ? row1 : row0; }
+    __device__ __forceinline__ int n(int t) const { return t ? n1 : n0; }
+    __device__ __forceinline__ int nmax() const { return n0 > n1 ? n0 : n1; }
+};
+
+__device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
+    Unit w;
+    const int inner_count = p.B * p.n_head_units;
+    const int ru = u / inner_count;
+    const int inner = u % inner_count;
+    w.b = inner / p.n_head_units;
+    const int hu = inner % p.n_head_units;
+    const int row_unit = p.causal ? (p.n_row_units - 1 - ru) : ru;
+    if (p.head_pairs) {
+        w.hq0 = 2 * hu;
+        w.hq1 = 2 * hu + 1;
+        w.row0 = w.row1 = row_unit * kBM;
+    } else {
+        w.hq0 = w.hq1 = hu;
+        w.row0 = row_unit * (kTiles * kBM);
+        w.row1 = w.row0 + kBM;
+    }
+    w.hkv = w.hq0 / (p.Hq / p.Hkv);
+    w.n0 = kv_tiles_for(p, w.row0);
+    w.n1 = kv_tiles_for(p, w.row1);
+    return w;
+}
+
+// j-th unit of this CTA in the snake order, or -1 when there is none.
+__device__ __forceinline__ int unit_of(const FwdParams& p, int j) {
+    const int G = static_cast<int>(gridDim.x);
+    const int c = static_cast<int>(blockIdx.x);
+    const long long u = (long long)j * G + ((j & 1) ? (G - 1 - c) : c);
+    return u < p.n_units ? static_cast<int>(u) : -1;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     fmha_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                    const FwdParams p) {
+                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
     extern __shared__ uint8_t smem_raw[];
     // align in the shared window (swizzle atoms and TMA boxes want 1024 bytes)
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -160,31 +224,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kSmemTmemSlot);
     auto bar = [&](int i) -> uint32_t { return sbase + kSmemBar + 8 * i; };
 
-    // ---- work unit of this CTA (longest causal row units first)
-    const int inner_count = p.B * p.n_head_units;
-    const int ru = static_cast<int>(blockIdx.x) / inner_count;
-    const int inner = static_cast<int>(blockIdx.x) % inner_count;
-    const int b = inner / p.n_head_units;
-    const int hu = inner % p.n_head_units;
-    const int row_unit = p.causal ? (p.n_row_units - 1 - ru) : ru;
-    int hq_t[kTiles], row0_t[kTiles], n_t[kTiles];
-    if (p.head_pairs) {
-        hq_t[0] = 2 * hu;
-        hq_t[1] = 2 * hu + 1;
-        row0_t[0] = row0_t[1] = row_unit * kBM;
-    } else {
-        hq_t[0] = hq_t[1] = hu;
-        row0_t[0] = row_unit * (kTiles * kBM);
-        row0_t[1] = row0_t[0] + kBM;
-    }
-    const int hkv = hq_t[0] / (p.Hq / p.Hkv);
-    n_t[0] = kv_tiles_for(p, row0_t[0]);
-    n_t[1] = kv_tiles_for(p, row0_t[1]);
-    const int n_max = max(n_t[0], n_t[1]);
-
     // ---- set-up: barriers, abort flag, tensor memory
     if (warp == kLoadWarp && lane == 0) {
-        mbar_init(bar(BAR_Q), 1);
+        for (int t = 0; t < kTiles; ++t) {
+            mbar_init(bar(BAR_QFULL + t), 1);
+            mbar_init(bar(BAR_QEMPTY + t), 1);
+            mbar_init(bar(BAR_SFULL + t), 1);
+            mbar_init(bar(BAR_PFULL + t), 4 * 32);
+            mbar_init(bar(BAR_ODONE + t), 1);
+            mbar_init(bar(BAR_OFREE + t), 4 * 32);
+        }
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(bar(BAR_KFULL + s), 1);
             mbar_init(bar(BAR_KEMPTY + s), 1);
@@ -193,18 +242,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(BAR_VFULL + s), 1);
             mbar_init(bar(BAR_VEMPTY + s), 1);
         }
-        for (int t = 0; t < kTiles; ++t) {
-            mbar_init(bar(BAR_SFULL + t), 1);
-            mbar_init(bar(BAR_PFULL + t), 4 * 32);
-            mbar_init(bar(BAR_ODONE + t), 1);
-        }
         mbar_init(bar(BAR_MMADONE), 1);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
-        tma_prefetch_desc(&tm_o);
     }
     if (warp == 0) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -221,112 +264,197 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             const uint64_t pol_q = l2_policy_evict_first();
             const uint64_t pol_kv = l2_policy_evict_last();
-            mbar_arrive_expect_tx(bar(BAR_Q), kTiles * kTileBytes);
-            for (int t = 0; t < kTiles; ++t)
-                for (int h = 0; h < 2; ++h)
-                    tma_load_4d(sbase + kSmemQ + t * kTileBytes + h * kHalfBytes, &tm_q, h * 64,
-                                hq_t[t], row0_t[t], b, bar(BAR_Q), pol_q);
-            int k_fills = 0, v_fills = 0;
-            for (int kt = 0; kt < n_max; ++kt) {
-                const int ks = kt % kKStages, kuse = kt / kKStages;
-                if (kuse > 0 && !wait_bounded(bar(BAR_KEMPTY + ks), (kuse - 1) & 1, abort_flag, limit))
-                    break;
-                mbar_arrive_expect_tx(bar(BAR_KFULL + ks), kTileBytes);
-                for (int h = 0; h < 2; ++h)
-                    tma_load_4d(sbase + kSmemK + ks * kTileBytes + h * kHalfBytes, &tm_k, h * 64,
-                                hkv, kt * kBN, b, bar(BAR_KFULL + ks), pol_kv);
-                ++k_fills;
-                const int vs = kt % kVStages, vuse = kt / kVStages;
-                if (vuse > 0 && !wait_bounded(bar(BAR_VEMPTY + vs), (vuse - 1) & 1, abort_flag, limit))
-                    break;
-                mbar_arrive_expect_tx(bar(BAR_VFULL + vs), kTileBytes);
-                for (int h = 0; h < 2; ++h)
-                    tma_load_4d(sbase + kSmemV + vs * kTileBytes + h * kHalfBytes, &tm_v, h * 64,
-                                hkv, kt * kBN, b, bar(BAR_VFULL + vs), pol_kv);
-                ++v_fills;
+            int k_issued = 0, v_issued = 0;  // KV ring fills issued so far
+            int q_issued[kTiles] = {0, 0};   // Q_t fills issued so far
+            bool ok = true;
+            for (int j = 0; ok; ++j) {
+                const int u = unit_of(p, j);
+                if (u < 0) break;
+                const Unit w = decode_unit(p, u);
+                for (int t = 0; t < kTiles; ++t) {
+                    // Q_t of the previous unit must be consumed by its last S_t MMA
+                    if (j > 0 && !wait_bounded(bar(BAR_QEMPTY + t), (j - 1) & 1, abort_flag, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar(BAR_QFULL + t), kTileBytes);
+                    for (int h = 0; h < 2; ++h)
+                        tma_load_4d(sbase + kSmemQ + t * kTileBytes + h * kHalfBytes, &tm_q, h * 64,
+                                    w.hq(t), w.row(t), w.b, bar(BAR_QFULL + t), pol_q);
+                    ++q_issued[t];
+                }
+                if (!ok) break;
+                const int nm = w.nmax();
+                for (int kt = 0; kt < nm; ++kt) {
+                    const int ks = k_issued % kKStages, kuse = k_issued / kKStages;
+                    if (kuse > 0 && !wait_bounded(bar(BAR_KEMPTY + ks), (kuse - 1) & 1, abort_flag, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar(BAR_KFULL + ks), kTileBytes);
+                    for (int h = 0; h < 2; ++h)
+                        tma_load_4d(sbase + kSmemK + ks * kTileBytes + h * kHalfBytes, &tm_k, h * 64,
+                                    w.hkv, kt * kBN, w.b, bar(BAR_KFULL + ks), pol_kv);
+                    ++k_issued;
+                    const int vs = v_issued % kVStages, vuse = v_issued / kVStages;
+                    if (vuse > 0 && !wait_bounded(bar(BAR_VEMPTY + vs), (vuse - 1) & 1, abort_flag, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar(BAR_VFULL + vs), kTileBytes);
+                    for (int h = 0; h < 2; ++h)
+                        tma_load_4d(sbase + kSmemV + vs * kTileBytes + h * kHalfBytes, &tm_v, h * 64,
+                                    w.hkv, kt * kBN, w.b, bar(BAR_VFULL + vs), pol_kv);
+                    ++v_issued;
+                }
             }
             // drain: every copy this thread issued has landed before the CTA may exit
-            drain_bounded(bar(BAR_Q), 0, limit);
+            for (int t = 0; t < kTiles; ++t)
+                if (q_issued[t] > 0) drain_bounded(bar(BAR_QFULL + t), (q_issued[t] - 1) & 1, limit);
             for (int s = 0; s < kKStages; ++s) {
-                const int fills = k_fills > s ? (k_fills - 1 - s) / kKStages + 1 : 0;
+                const int fills = k_issued > s ? (k_issued - 1 - s) / kKStages + 1 : 0;
                 if (fills) drain_bounded(bar(BAR_KFULL + s), (fills - 1) & 1, limit);
             }
             for (int s = 0; s < kVStages; ++s) {
-                const int fills = v_fills > s ? (v_fills - 1 - s) / kVStages + 1 : 0;
+                const int fills = v_issued > s ? (v_issued - 1 - s) / kVStages + 1 : 0;
                 if (fills) drain_bounded(bar(BAR_VFULL + s), (fills - 1) & 1, limit);
             }
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
         // =========================== MMA issuer =============================
-        if (lane == 0 && n_max > 0) {
-            constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, false);
-            constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, kHeadDim, true);
-            auto issue_qk = [&](int t, int ks) {
-                const uint32_t d = tmem_base + kTmemS + 128 * t;
-                const uint32_t qa = sbase + kSmemQ + t * kTileBytes;
-                const uint32_t kb = sbase + kSmemK + ks * kTileBytes;
+        // The whole warp runs the control flow (so descriptors and stage indices stay
+        // warp-uniform); one elected lane issues each group of MMAs and its commits.
+        constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, false);
+        constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, kHeadDim, true);
+        // descriptor of k-step kk = base descriptor + constant start-address offset (>> 4)
+        const uint64_t q_desc0 = sdesc_sw128(sbase + kSmemQ, 16, 1024);
+        const uint64_t k_desc0 = sdesc_sw128(sbase + kSmemK, 16, 1024);
+        const uint64_t v_desc0 = sdesc_sw128(sbase + kSmemV, kHalfBytes, 1024);
+        auto issue_qk = [&](int t, int ks) {
+            const uint32_t d = tmem_base + kTmemS + 128 * t;
+            const uint64_t qd = q_desc0 + static_cast<uint64_t>((t * kTileBytes) >> 4);
+            const uint64_t kd = k_desc0 + static_cast<uint64_t>((ks * kTileBytes) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                    mma_bf16_ss(d, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
-                                idesc_qk, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+                const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
+                mma_bf16_ss(d, qd + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
+            }
+        };
+        auto issue_pv = [&](int t, int vs, bool accumulate) {
+            const uint32_t d = tmem_base + kTmemO + 128 * t;
+            const uint32_t pa = tmem_base + kTmemS + 128 * t;
+            const uint64_t vd = v_desc0 + static_cast<uint64_t>((vs * kTileBytes) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < kBN / 16; ++kk)
+                mma_bf16_ts(d, pa + kk * 8, vd + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc_pv,
+                            (accumulate || kk > 0) ? 1u : 0u);
+        };
+        int kv = 0;                 // KV tiles consumed so far (ring position)
+        int sc0 = 0, sc1 = 0;       // S_t products issued so far (s_full / p_full phase)
+        bool ok = true;
+        for (int j = 0; ok; ++j) {
+            const int u = unit_of(p, j);
+            if (u < 0) break;
+            const Unit w = decode_unit(p, u);
+            const int nm = w.nmax();
+            // S_t(0) for each tile that has work; Q_t must have landed
+            bool k_ready = false;
+            for (int t = 0; t < kTiles && ok; ++t) {
+                ok = wait_bounded(bar(BAR_QFULL + t), j & 1, abort_flag, limit);
+                if (!ok) break;
+                if (w.n(t) > 0 && !k_ready) {
+                    ok = wait_bounded(bar(BAR_KFULL + kv % kKStages), (kv / kKStages) & 1, abort_flag, limit);
+                    if (!ok) break;
+                    k_ready = true;
                 }
-            };
-            auto issue_pv = [&](int t, int vs, bool accumulate) {
-                const uint32_t d = tmem_base + kTmemO + 128 * t;
-                const uint32_t pa = tmem_base + kTmemS + 128 * t;
-                const uint32_t vb = sbase + kSmemV + vs * kTileBytes;
-#pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk)
-                    mma_bf16_ts(d, pa + kk * 8, sdesc_sw128(vb + kk * 16 * 128, kHalfBytes, 1024),
-                                idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
-            };
-            bool ok = wait_bounded(bar(BAR_Q), 0, abort_flag, limit) &&
-                      wait_bounded(bar(BAR_KFULL + 0), 0, abort_flag, limit);
-            if (ok) {
                 tc_fence_after();
-                for (int t = 0; t < kTiles; ++t)
-                    if (n_t[t] > 0) {
-                        issue_qk(t, 0);
+                if (elect_one()) {
+                    if (w.n(t) > 0) {
+                        issue_qk(t, kv % kKStages);
                         mma_commit(bar(BAR_SFULL + t));
                     }
-                mma_commit(bar(BAR_KEMPTY + 0));
+                    if (w.n(t) <= 1) mma_commit(bar(BAR_QEMPTY + t));  // Q_t no longer read
+                }
+                __syncwarp();
+                if (w.n(t) > 0) {
+                    if (t == 0) ++sc0; else ++sc1;
+                }
             }
-            for (int kt = 0; ok && kt < n_max; ++kt) {
-                const int vs = kt % kVStages, vuse = kt / kVStages;
-                const int ks = (kt + 1) % kKStages, kuse = (kt + 1) / kKStages;
-                if (!wait_bounded(bar(BAR_VFULL + vs), vuse & 1, abort_flag, limit)) break;
-                tc_fence_after();
-                bool k_ready = false;
-                for (int t = 0; ok && t < kTiles; ++t) {
-                    if (kt < n_t[t]) {
-                        if (!wait_bounded(bar(BAR_PFULL + t), kt & 1, abort_flag, limit)) {
+            if (!ok) break;
+            if (nm > 0) {
+                if (elect_one()) mma_commit(bar(BAR_KEMPTY + kv % kKStages));
+                __syncwarp();
+            }
+            for (int kt = 0; ok && kt < nm; ++kt) {
+                const int vs = kv % kVStages, vuse = kv / kVStages;
+                const int kn = kv + 1;  // ring position of K_{kt+1}
+                if (!wait_bounded(bar(BAR_VFULL + vs), vuse & 1, abort_flag, limit)) {
+                    ok = false;
+                    break;
+                }
+                bool kn_ready = false;
+                for (int t = 0; t < kTiles; ++t) {
+                    const int nt = w.n(t);
+                    if (kt < nt) {
+                        const int sc = t ? sc1 : sc0;
+                        // P_t(kt) written by the softmax warpgroup
+                        if (!wait_bounded(bar(BAR_PFULL + t), (sc - 1) & 1, abort_flag, limit)) {
+                            ok = false;
+                            break;
+                        }
+                        // the first P.V of a unit overwrites O_t: the previous unit's
+                        // epilogue must have read it out of tensor memory
+                        if (kt == 0 && j > 0 &&
+                            !wait_bounded(bar(BAR_OFREE + t), (j - 1) & 1, abort_flag, limit)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        issue_pv(t, vs, kt > 0);
-                        if (kt == n_t[t] - 1) mma_commit(bar(BAR_ODONE + t));
+                        if (elect_one()) {
+                            issue_pv(t, vs, kt > 0);
+                            if (kt == nt - 1) mma_commit(bar(BAR_ODONE + t));  // O_t final
+                        }
+                        __syncwarp();
+                    } else if (nt == 0 && kt == 0) {
+                        if (elect_one()) mma_commit(bar(BAR_ODONE + t));  // tile without work
+                        __syncwarp();
                     }
-                    if (kt + 1 < n_t[t]) {
-                        if (!k_ready) {
-                            if (!wait_bounded(bar(BAR_KFULL + ks), kuse & 1, abort_flag, limit)) {
+                    if (kt + 1 < nt) {
+                        if (!kn_ready) {
+                            if (!wait_bounded(bar(BAR_KFULL + kn % kKStages), (kn / kKStages) & 1, abort_flag,
+                                              limit)) {
                                 ok = false;
                                 break;
                             }
                             tc_fence_after();
-                            k_ready = true;
+                            kn_ready = true;
                         }
-                        issue_qk(t, ks);
-                        mma_commit(bar(BAR_SFULL + t));
+                        if (elect_one()) {
+                            issue_qk(t, kn % kKStages);
+                            mma_commit(bar(BAR_SFULL + t));
+                            if (kt + 2 == nt) mma_commit(bar(BAR_QEMPTY + t));  // last S_t of the unit
+                        }
+                        __syncwarp();
+                        if (t == 0) ++sc0; else ++sc1;
                     }
                 }
                 if (!ok) break;
-                mma_commit(bar(BAR_VEMPTY + vs));
-                if (kt + 1 < n_max) mma_commit(bar(BAR_KEMPTY + ks));
+                if (elect_one()) {
+                    mma_commit(bar(BAR_VEMPTY + vs));
+                    if (kt + 1 < nm) mma_commit(bar(BAR_KEMPTY + kn % kKStages));
+                }
+                __syncwarp();
+                ++kv;
             }
-            // every MMA this thread issued has completed before tensor memory is freed
+            if (ok && nm == 0) {
+                if (elect_one())
+                    for (int t = 0; t < kTiles; ++t) mma_commit(bar(BAR_ODONE + t));
+                __syncwarp();
+            }
+        }
+        // every MMA this warp issued has completed before tensor memory is freed
+        if (elect_one()) {
             mma_commit(bar(BAR_MMADONE));
             drain_bounded(bar(BAR_MMADONE), 0, limit);
         }
@@ -339,128 +467,190 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const uint32_t tS = tmem_base + lane_off + kTmemS + 128 * t;
         const uint32_t tO = tmem_base + lane_off + kTmemO + 128 * t;
-        const int row = row0_t[t] + r;
-        const int nt = n_t[t];
-        // last key this row may see
-        const long long lim_ll =
-            p.causal ? min((long long)row + (p.Skv - p.Sq), (long long)p.Skv - 1) : (long long)p.Skv - 1;
-        const int lim = static_cast<int>(lim_ll < -1 ? -1 : lim_ll);
         const float sl2 = p.scale_log2;
-        float m_run = -INFINITY;  // running max (log2 units of scaled logits) used by the weights
-        float l_run = 0.f;        // running sum of weights
+        int sc = 0;  // S_t products consumed so far
         bool ok = true;
 
-        for (int kt = 0; kt < nt; ++kt) {
-            // warp-uniform outcome: the tcgen05.ld/st below are warp-collective
-            const bool got = wait_bounded(bar(BAR_SFULL + t), kt & 1, abort_flag, limit);
+        for (int j = 0; ok; ++j) {
+            const int u = unit_of(p, j);
+            if (u < 0) break;
+            const Unit w = decode_unit(p, u);
+            const int nt = w.n(t);
+            const int row = w.row(t) + r;
+            const long long lim_ll = p.causal ? min((long long)row + (p.Skv - p.Sq), (long long)p.Skv - 1)
+                                              : (long long)p.Skv - 1;
+            const int lim = static_cast<int>(lim_ll < -1 ? -1 : lim_ll);  // last visible key
+            float m_run = -INFINITY;  // running max (log2 units of scaled logits) used by the weights
+            float l_run = 0.f;        // running sum of weights
+
+            for (int kt = 0; kt < nt; ++kt, ++sc) {
+                // warp-uniform outcome: the tcgen05.ld/st below are warp-collective
+                const bool got = wait_bounded(bar(BAR_SFULL + t), sc & 1, abort_flag, limit);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t s[128];
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&s[32 * c]));
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_wait_ld_regs(*reinterpret_cast<uint32_t(*)[32]>(&s[32 * c]));
+
+                const int nvis = lim - kt * kBN + 1;  // visible keys of this row in the tile
+                if (nvis < kBN) {
+#pragma unroll
+                    for (int jj = 0; jj < kBN; ++jj)
+                        if (jj >= nvis) s[jj] = __float_as_uint(-INFINITY);
+                }
+                // tile maximum (three-input max, 8 independent chains)
+                float mx[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    mx[q] = fmax3(__uint_as_float(s[q]), __uint_as_float(s[8 + q]), __uint_as_float(s[16 + q]));
+#pragma unroll
+                for (int base = 24; base < kBN; base += 16)
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        mx[q] = fmax3(mx[q], __uint_as_float(s[base + q]), __uint_as_float(s[base + 8 + q]));
+                const float tmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                         fmaxf(mx[6], mx[7]));
+                const float m_tile = tmax * sl2;
+
+                // weights 2^(s*scale*log2e - m_use) and their row sum; packed to bf16
+                // pairs and stored as P_t chunk by chunk (32 weights = 16 columns)
+                float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
+                auto weights = [&](float m_use) {
+                    rs0 = rs1 = rs2 = rs3 = 0.f;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int q = 0; q < 16; q += 2) {
+                            const int e = 32 * c + 2 * q;
+                            float a0, a1, b0, b1;
+                            ffma2_bc(a0, a1, __uint_as_float(s[e]), __uint_as_float(s[e + 1]), sl2, -m_use);
+                            ffma2_bc(b0, b1, __uint_as_float(s[e + 2]), __uint_as_float(s[e + 3]), sl2, -m_use);
+                            a0 = ex2_approx(a0);
+                            a1 = ex2_approx(a1);
+                            b0 = ex2_approx(b0);
+                            b1 = ex2_approx(b1);
+                            if (q & 2) {
+                                fadd2_acc(rs2, rs3, a0, a1);
+                                fadd2_acc(rs2, rs3, b0, b1);
+                            } else {
+                                fadd2_acc(rs0, rs1, a0, a1);
+                                fadd2_acc(rs0, rs1, b0, b1);
+                            }
+                            pk[q] = pack_bf16x2(a0, a1);
+                            pk[q + 1] = pack_bf16x2(b0, b1);
+                        }
+                        tmem_st16(tS + 16 * c, pk);
+                    }
+                };
+                float alpha = 1.f;
+#if ATTN_SPECULATIVE_EXP
+                // against the running max, known before the tile maximum is reduced
+                // (weights() stores to TMEM warp-collectively: every call is warp-uniform)
+                const bool rise = m_tile - m_run > kRescaleLog2;  // rare after the first tile
+                if (__all_sync(0xffffffffu, m_run == -INFINITY)) {
+                    // first tile of the warp's rows: nothing to speculate on
+                    if (rise) {
+                        alpha = ex2_approx(m_run - m_tile);
+                        m_run = m_tile;
+                    }
+                    weights(m_run == -INFINITY ? 0.f : m_run);
+                } else {
+                    weights(m_run == -INFINITY ? 0.f : m_run);
+                    if (rise) {
+                        alpha = ex2_approx(m_run - m_tile);
+                        m_run = m_tile;
+                    }
+                    if (__any_sync(0xffffffffu, rise)) {
+                        tmem_wait_st();  // the first stores land before they are overwritten
+                        weights(m_run == -INFINITY ? 0.f : m_run);
+                    }
+                }
+#else
+                if (m_tile - m_run > kRescaleLog2) {  // the max rose past 2^8 (always on the
+                    alpha = ex2_approx(m_run - m_tile);  // first visible tile: alpha = 0)
+                    m_run = m_tile;
+                }
+                weights(m_run == -INFINITY ? 0.f : m_run);
+#endif
+                l_run = l_run * alpha + ((rs0 + rs1) + (rs2 + rs3));
+                // O_t holds P.V of tiles < kt (complete: S_t(kt) was issued after them)
+                const bool need = (kt > 0) && (alpha != 1.f);
+                if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + 32 * c, o);
+                        tmem_wait_ld_regs(o);
+#pragma unroll
+                        for (int q = 0; q < 32; q += 2) {
+                            float x0, x1;
+                            fmul2_b(x0, x1, __uint_as_float(o[q]), __uint_as_float(o[q + 1]), alpha);
+                            o[q] = __float_as_uint(x0);
+                            o[q + 1] = __float_as_uint(x1);
+                        }
+                        tmem_st32(tO + 32 * c, o);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar(BAR_PFULL + t));
+            }
+            if (!ok) break;
+
+            // ------------------------------ epilogue ------------------------------
+            // O_t is final once every P.V of this unit completed
+            const bool got = wait_bounded(bar(BAR_ODONE + t), j & 1, abort_flag, limit);
             if (!__all_sync(0xffffffffu, got)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            uint32_t s[128];
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-                tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&s[32 * c]));
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_wait_ld_regs(*reinterpret_cast<uint32_t(*)[32]>(&s[32 * c]));
-
-            const int nvis = lim - kt * kBN + 1;  // visible keys of this row in the tile
-            if (nvis < kBN) {
-#pragma unroll
-                for (int j = 0; j < kBN; ++j)
-                    if (j >= nvis) s[j] = __float_as_uint(-INFINITY);
-            }
-            float mx[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) mx[u] = __uint_as_float(s[u]);
-#pragma unroll
-            for (int j = 8; j < kBN; ++j) mx[j & 7] = fmaxf(mx[j & 7], __uint_as_float(s[j]));
-            const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                     fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-            const float m_tile = tmax * sl2;
-            float alpha = 1.f;
-            if (m_tile - m_run > kRescaleLog2) {  // false while both are -inf
-                alpha = ex2_approx(m_run - m_tile);
-                m_run = m_tile;
-            }
-            const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-            float rs[4] = {0.f, 0.f, 0.f, 0.f};
+            // O_t -> registers 32 columns at a time -> (1/l) -> bf16 -> global (this row's
+            // 256 bytes); the last TMEM load frees O_t for the next unit's first P.V
+            const bool store = row < p.Sq;
+            const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+            uint4* dst = reinterpret_cast<uint4*>(
+                p.o + ((static_cast<size_t>(w.b) * p.Sq + (store ? row : 0)) * p.Hq + w.hq(t)) * kHeadDim);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(s[32 * c + 2 * u]), sl2, -m_use));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(s[32 * c + 2 * u + 1]), sl2, -m_use));
-                    rs[c] += p0 + p1;
-                    pk[u] = pack_bf16x2(p0, p1);
-                }
-                tmem_st16(tS + 16 * c, pk);
-            }
-            l_run = l_run * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
-            // O_t holds P.V of tiles < kt (complete: S_t(kt) was issued after them)
-            const bool need = (kt > 0) && (alpha != 1.f);
-            if (__any_sync(0xffffffffu, need)) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t o[32];
+                uint32_t o[32];
+                if (nt > 0) {
                     tmem_ld32(tO + 32 * c, o);
                     tmem_wait_ld_regs(o);
+                } else {
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
-                    tmem_st32(tO + 32 * c, o);
+                    for (int e = 0; e < 32; ++e) o[e] = 0u;
+                }
+                if (c == 3) {
+                    tc_fence_before();
+                    mbar_arrive(bar(BAR_OFREE + t));
+                }
+                if (store) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        float f[8];
+#pragma unroll
+                        for (int e = 0; e < 8; e += 2)
+                            fmul2_b(f[e], f[e + 1], __uint_as_float(o[8 * q + e]),
+                                    __uint_as_float(o[8 * q + e + 1]), inv_l);
+                        dst[4 * c + q] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                                                    pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+                    }
                 }
             }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(bar(BAR_PFULL + t));
-        }
-
-        // ------------------------------ epilogue ------------------------------
-        bool have = ok && nt > 0;
-        if (have) have = wait_bounded(bar(BAR_ODONE + t), 0, abort_flag, limit);
-        have = __all_sync(0xffffffffu, have);
-        // the staging buffer is Q_t's: its TMA load must have landed (it may never
-        // have been waited on when this tile had no KV tile to visit)
-        drain_bounded(bar(BAR_Q), 0, limit);
-        tc_fence_after();
-        const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
-        uint8_t* stage = smem + kSmemQ + t * kTileBytes;  // Q_t is dead once O_t is final
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            uint32_t o[32];
-            if (have) {
-                tmem_ld32(tO + 32 * c, o);
-                tmem_wait_ld_regs(o);
-            } else {
-#pragma unroll
-                for (int u = 0; u < 32; ++u) o[u] = 0u;
+            if (store) {
+                if (p.lse != nullptr) {
+                    const float lse = l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+                    p.lse[(static_cast<size_t>(w.b) * p.Hq + w.hq(t)) * p.Sq + row] = lse;
+                }
             }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                uint4 val;
-                val.x = pack_bf16x2(__uint_as_float(o[8 * u + 0]) * inv_l, __uint_as_float(o[8 * u + 1]) * inv_l);
-                val.y = pack_bf16x2(__uint_as_float(o[8 * u + 2]) * inv_l, __uint_as_float(o[8 * u + 3]) * inv_l);
-                val.z = pack_bf16x2(__uint_as_float(o[8 * u + 4]) * inv_l, __uint_as_float(o[8 * u + 5]) * inv_l);
-                val.w = pack_bf16x2(__uint_as_float(o[8 * u + 6]) * inv_l, __uint_as_float(o[8 * u + 7]) * inv_l);
-                const int half = c >> 1;
-                const int chunk = (c & 1) * 4 + u;       // 16-byte chunk within the 128-byte row
-                const int phys = chunk ^ (r & 7);         // 128-byte swizzle
-                *reinterpret_cast<uint4*>(stage + half * kHalfBytes + r * 128 + phys * 16) = val;
-            }
-        }
-        if (p.lse != nullptr && row < p.Sq) {
-            const float lse = l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
-            p.lse[(static_cast<size_t>(b) * p.Hq + hq_t[t]) * p.Sq + row] = lse;
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(1 + t, 128);
-        if (r == 0 && row0_t[t] < p.Sq && *abort_flag == 0) {
-            for (int h = 0; h < 2; ++h)
-                tma_store_4d(&tm_o, smem_u32(stage + h * kHalfBytes), h * 64, hq_t[t], row0_t[t], b);
-            bulk_commit_group();
-            bulk_wait_group0();
         }
     }
 

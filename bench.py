@@ -173,16 +173,37 @@ def oracle_sample_rate(w, target_s: float, seed: int = 0, q=None, k=None, v=None
         vis = np.minimum(w.Skv, rows[:, 2] + off + 1) if w.causal else np.full(len(rows), w.Skv)
         return float(4 * w.D * np.maximum(vis, 0).sum())
 
-    probe = rows_of(32)
-    t0 = time.perf_counter()
-    oracle.attn_rows(q, k, v, probe, bool(w.causal), w.scale)
-    dt = max(time.perf_counter() - t0, 1e-4)
-    n = int(max(32, min(2_000_000, 32 * target_s / dt)))
+    # calibrate: double the probe until it runs for ~1/8 of the target
+    n, dt = 64, 0.0
+    while True:
+        t0 = time.perf_counter()
+        oracle.attn_rows(q, k, v, rows_of(n), bool(w.causal), w.scale)
+        dt = time.perf_counter() - t0
+        if dt >= target_s / 8 or n >= 1_000_000:
+            break
+        n *= 2
+    n = int(max(64, min(4_000_000, n * target_s / max(dt, 1e-4))))
     rows = rows_of(n)
     t0 = time.perf_counter()
     oracle.attn_rows(q, k, v, rows, bool(w.causal), w.scale)
     dt = time.perf_counter() - t0
     return flops_of(rows) / dt / 1e12, dt, n, oracle.num_threads()
+
+
+# ------------------------------------------------------------------ multi-rank helpers
+def max_over_ranks(values, device):
+    """Element-wise max of `values` over all ranks of the default process group."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_tflops(world: int, flops_per_step: int, steps: int, seconds: float) -> float:
+    """Whole-job throughput: every rank ran `steps` steps of `flops_per_step`;
+    `seconds` is the slowest rank's timed region."""
+    return world * flops_per_step * steps / seconds / 1e12
 
 
 # ------------------------------------------------------------------ main arms
@@ -323,16 +344,14 @@ def run_ours(args, w):
     e2e_s = e_start.elapsed_time(e_end) / 1e3
 
     if world > 1:
-        t = torch.tensor([kernel_s, e2e_s], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        kernel_s, e2e_s = float(t[0]), float(t[1])
+        kernel_s, e2e_s = max_over_ranks([kernel_s, e2e_s], dev)
         dist.destroy_process_group()
     if rank != 0:
         return
 
     flops = metric_flops(w)
-    value = world * flops * args.steps / kernel_s / 1e12
-    e2e_value = world * flops * e2e_steps / e2e_s / 1e12
+    value = job_tflops(world, flops, args.steps, kernel_s)
+    e2e_value = job_tflops(world, flops, e2e_steps, e2e_s)
     peak, peak_kind = load_peaks()
     exact = exact_flops(w)
     mean_launch_s = kernel_s / args.steps
