@@ -129,9 +129,9 @@ extern "C" attn_status_t attn_fwd(const void* q, const void* k, const void* v, v
     p.n_units = static_cast<int>(n_units);
     p.o = static_cast<uint16_t*>(o);
 
-    CUtensorMap tm_q, tm_k, tm_v;
+    CUtensorMap tm_q, tm_k, tm_v, tm_o;
     if (!encode_bshd(&tm_q, q, B, Sq, Hq, D) || !encode_bshd(&tm_k, k, B, Skv, Hkv, D) ||
-        !encode_bshd(&tm_v, v, B, Skv, Hkv, D))
+        !encode_bshd(&tm_v, v, B, Skv, Hkv, D) || !encode_bshd(&tm_o, o, B, Sq, Hq, D))
         return ATTN_ERR_CUDA;
 
     int dev = 0, sms = 0;
@@ -139,7 +139,7 @@ extern "C" attn_status_t attn_fwd(const void* q, const void* k, const void* v, v
     // persistent grid: at most one CTA per SM (the CTA holds all 512 TMEM columns)
     const int grid = static_cast<int>(n_units < sms ? n_units : sms);
     attn::fmha_fwd_kernel<<<static_cast<unsigned int>(grid), attn::kThreads, attn::kSmemBytes,
-                            stream>>>(tm_q, tm_k, tm_v, p);
+                            stream>>>(tm_q, tm_k, tm_v, tm_o, p);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return ATTN_OK;

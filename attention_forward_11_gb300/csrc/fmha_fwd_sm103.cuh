@@ -10,12 +10,18 @@
 // (round r: CTA c takes unit r*G + c, or r*G + G-1-c on odd rounds), so the
 // next unit's Q is loaded while the current one finishes.
 //
-// Warp roles (320 threads):
-//   warps 0-3  softmax warpgroup of tile 0 (one query row per thread)
-//   warps 4-7  softmax warpgroup of tile 1
-//   warp  8    MMA issuer (one elected lane): S_t = Q_t K^T and O_t += P_t V on tcgen05
-//   warp  9    TMA producer (one thread): Q of each unit, K and V tiles through
-//              two shared-memory rings guarded by full/empty mbarriers
+// Warp roles (512 threads, four warpgroups):
+//   warps 0-3    softmax warpgroup of tile 0 (one query row per thread)
+//   warps 4-7    softmax warpgroup of tile 1
+//   warps 8-11   epilogue warpgroup: O_t out of tensor memory, times 1/l, bf16,
+//                TMA store; LSE.  It runs while the softmax warpgroups start the
+//                next unit, so the store never sits on the softmax critical path.
+//   warp  12     MMA issuer (one elected lane): S_t = Q_t K^T and O_t += P_t V
+//   warp  13     TMA producer (one thread): Q of each unit (plus an L2 prefetch of
+//                the next unit's Q), K and V tiles through two shared-memory rings
+//   warps 14-15  idle
+// Registers are split with setmaxnreg: softmax 176, epilogue 88, MMA/producer 72
+// per thread (2*176 + 88 + 72 = 4 * 128, the launch allocation of 128 per thread).
 //
 // Tensor memory (512 columns x 128 lanes, fp32): S_0 | S_1 | O_0 | O_1, 128 columns
 // each.  P_t (bf16, two per column) is written over the first 64 columns of S_t
@@ -29,10 +35,8 @@
 // maximum exceeds it by more than 8 (log2 units); otherwise the stale maximum
 // is kept (weights stay <= 256; l and O share it, so the quotient is the same),
 // and O in tensor memory is rescaled only on the rare tiles that raise it.
-// (Optionally, ATTN_SPECULATIVE_EXP, the weights are computed against the stale
-// maximum while the tile maximum is still being reduced, and only rows whose
-// maximum rises recompute them; that keeps every logit live and needs more
-// registers per thread than this 10-warp layout leaves.)
+// The weights of a tile are handed to the MMA warp in two halves of 64 keys, so
+// the first half of O += P.V runs while the second half's exponentials are made.
 //
 // Causal (bottom-right aligned: key j visible from row i iff j <= i + Skv - Sq):
 // KV tiles entirely above a tile's last visible key are never loaded or
@@ -53,10 +57,7 @@
 #define ATTN_KSTAGES 2
 #endif
 #ifndef ATTN_VSTAGES
-#define ATTN_VSTAGES 3
-#endif
-#ifndef ATTN_SPECULATIVE_EXP
-#define ATTN_SPECULATIVE_EXP 0  // weights against the stale max before the tile max is known
+#define ATTN_VSTAGES 2
 #endif
 
 namespace attn {
@@ -69,10 +70,14 @@ constexpr int kKStages = ATTN_KSTAGES;   // K ring depth
 constexpr int kVStages = ATTN_VSTAGES;   // V ring depth
 constexpr int kTileBytes = kBM * kHeadDim * 2;   // 32 KB bf16 tile (Q, K or V)
 constexpr int kHalfBytes = kTileBytes / 2;       // one 64-column, 128-byte-swizzled half
-constexpr int kSoftmaxWarps = 4 * kTiles;
-constexpr int kMmaWarp = kSoftmaxWarps;
-constexpr int kLoadWarp = kSoftmaxWarps + 1;
-constexpr int kThreads = 32 * (kSoftmaxWarps + 2);
+constexpr int kSoftmaxWarps = 4 * kTiles;          // warpgroups 0 and 1
+constexpr int kEpilogueWarp0 = kSoftmaxWarps;      // warpgroup 2
+constexpr int kMmaWarp = kEpilogueWarp0 + 4;       // warpgroup 3
+constexpr int kLoadWarp = kMmaWarp + 1;
+constexpr int kThreads = 512;
+constexpr int kRegsSoftmax = 176, kRegsEpilogue = 88, kRegsOther = 72;
+static_assert(2 * kRegsSoftmax + kRegsEpilogue + kRegsOther <= 4 * (65536 / kThreads),
+              "register split exceeds the launch allocation");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 0;           // S_t at kTmemS + 128 t
 constexpr uint32_t kTmemO = 256;         // O_t at kTmemO + 128 t
@@ -82,7 +87,9 @@ constexpr float kRescaleLog2 = 8.0f;     // raise the running max only past 2^8
 constexpr int kSmemQ = 0;
 constexpr int kSmemK = kSmemQ + kTiles * kTileBytes;
 constexpr int kSmemV = kSmemK + kKStages * kTileBytes;
-constexpr int kSmemBar = kSmemV + kVStages * kTileBytes;
+constexpr int kSmemStage = kSmemV + kVStages * kTileBytes;  // O staging: one 64-column half
+constexpr int kSmemStats = kSmemStage + kHalfBytes;           // per tile and row: (m, l)
+constexpr int kSmemBar = kSmemStats + kTiles * kBM * 8;
 enum : int {
     BAR_QFULL = 0,
     BAR_QEMPTY = BAR_QFULL + kTiles,
@@ -91,10 +98,12 @@ enum : int {
     BAR_VFULL = BAR_KEMPTY + kKStages,
     BAR_VEMPTY = BAR_VFULL + kVStages,
     BAR_SFULL = BAR_VEMPTY + kVStages,
-    BAR_PFULL = BAR_SFULL + kTiles,
-    BAR_ODONE = BAR_PFULL + kTiles,
+    BAR_PFULL = BAR_SFULL + kTiles,          // [tile][half]: P of 64 keys in TMEM
+    BAR_ODONE = BAR_PFULL + 2 * kTiles,
     BAR_OFREE = BAR_ODONE + kTiles,
-    BAR_MMADONE = BAR_OFREE + kTiles,
+    BAR_STATSFULL = BAR_OFREE + kTiles,
+    BAR_STATSFREE = BAR_STATSFULL + kTiles,
+    BAR_MMADONE = BAR_STATSFREE + kTiles,
     BAR_COUNT
 };
 constexpr int kSmemTmemSlot = kSmemBar + BAR_COUNT * 8;
@@ -140,6 +149,15 @@ __device__ __forceinline__ bool drain_bounded(uint32_t bar, uint32_t parity, uns
         if (mbar_try_wait(bar, parity)) return true;
     atomicOr(&g_attn_status, kStatusTimeout);
     return false;
+}
+
+__device__ __forceinline__ void tmem_wait_ld_regs16(uint32_t (&r)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]),
+                   "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+                 :
+                 : "memory");
 }
 
 // tcgen05.wait::ld that also orders the loaded registers after the wait
@@ -213,7 +231,8 @@ __device__ __forceinline__ int unit_of(const FwdParams& p, int j) {
 
 __global__ void __launch_bounds__(kThreads, 1)
     fmha_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                    const FwdParams p) {
     extern __shared__ uint8_t smem_raw[];
     // align in the shared window (swizzle atoms and TMA boxes want 1024 bytes)
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -230,9 +249,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(BAR_QFULL + t), 1);
             mbar_init(bar(BAR_QEMPTY + t), 1);
             mbar_init(bar(BAR_SFULL + t), 1);
-            mbar_init(bar(BAR_PFULL + t), 4 * 32);
+            mbar_init(bar(BAR_PFULL + 2 * t), 4 * 32);
+            mbar_init(bar(BAR_PFULL + 2 * t + 1), 4 * 32);
             mbar_init(bar(BAR_ODONE + t), 1);
             mbar_init(bar(BAR_OFREE + t), 4 * 32);
+            mbar_init(bar(BAR_STATSFULL + t), 4 * 32);
+            mbar_init(bar(BAR_STATSFREE + t), 4 * 32);
         }
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(bar(BAR_KFULL + s), 1);
@@ -248,6 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
+        tma_prefetch_desc(&tm_o);
     }
     if (warp == 0) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -258,8 +281,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const unsigned int limit = p.poll_limit;
+    const int wg = warp / 4;
 
-    if (warp == kLoadWarp) {
+    if (wg == 3) {
+      regs_dec<kRegsOther>();  // warpgroup-wide, before the warps take their roles
+      if (warp == kLoadWarp) {
         // =========================== TMA producer ===========================
         if (lane == 0) {
             const uint64_t pol_q = l2_policy_evict_first();
@@ -284,6 +310,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++q_issued[t];
                 }
                 if (!ok) break;
+                const int un = unit_of(p, j + 1);
+                if (un >= 0) {  // warm L2 with the next unit's Q while this unit runs
+                    const Unit wn = decode_unit(p, un);
+                    for (int t = 0; t < kTiles; ++t)
+                        for (int h = 0; h < 2; ++h) tma_prefetch_l2_4d(&tm_q, h * 64, wn.hq(t), wn.row(t), wn.b);
+                }
                 const int nm = w.nmax();
                 for (int kt = 0; kt < nm; ++kt) {
                     const int ks = k_issued % kKStages, kuse = k_issued / kKStages;
@@ -321,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
-    } else if (warp == kMmaWarp) {
+      } else if (warp == kMmaWarp) {
         // =========================== MMA issuer =============================
         // The whole warp runs the control flow (so descriptors and stage indices stay
         // warp-uniform); one elected lane issues each group of MMAs and its commits.
@@ -341,14 +373,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_bf16_ss(d, qd + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
             }
         };
-        auto issue_pv = [&](int t, int vs, bool accumulate) {
+        // O_t (+)= P_t V over keys [64 h, 64 h + 64) of the KV tile
+        auto issue_pv = [&](int t, int vs, int h, bool accumulate) {
             const uint32_t d = tmem_base + kTmemO + 128 * t;
             const uint32_t pa = tmem_base + kTmemS + 128 * t;
             const uint64_t vd = v_desc0 + static_cast<uint64_t>((vs * kTileBytes) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk)
+            for (int q = 0; q < kBN / 32; ++q) {
+                const int kk = h * (kBN / 32) + q;
                 mma_bf16_ts(d, pa + kk * 8, vd + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc_pv,
                             (accumulate || kk > 0) ? 1u : 0u);
+            }
         };
         int kv = 0;                 // KV tiles consumed so far (ring position)
         int sc0 = 0, sc1 = 0;       // S_t products issued so far (s_full / p_full phase)
@@ -398,11 +433,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int nt = w.n(t);
                     if (kt < nt) {
                         const int sc = t ? sc1 : sc0;
-                        // P_t(kt) written by the softmax warpgroup
-                        if (!wait_bounded(bar(BAR_PFULL + t), (sc - 1) & 1, abort_flag, limit)) {
-                            ok = false;
-                            break;
-                        }
                         // the first P.V of a unit overwrites O_t: the previous unit's
                         // epilogue must have read it out of tensor memory
                         if (kt == 0 && j > 0 &&
@@ -410,14 +440,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ok = false;
                             break;
                         }
-                        tc_fence_after();
-                        if (elect_one()) {
-                            issue_pv(t, vs, kt > 0);
-                            if (kt == nt - 1) mma_commit(bar(BAR_ODONE + t));  // O_t final
+                        // P_t(kt) arrives in two halves of 64 keys; each half's P.V starts
+                        // as soon as the softmax warpgroup has stored it
+                        for (int h = 0; h < 2; ++h) {
+                            if (!wait_bounded(bar(BAR_PFULL + 2 * t + h), (sc - 1) & 1, abort_flag, limit)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            if (elect_one()) {
+                                issue_pv(t, vs, h, kt > 0);
+                                if (h == 1 && kt == nt - 1) mma_commit(bar(BAR_ODONE + t));  // O_t final
+                            }
+                            __syncwarp();
                         }
-                        __syncwarp();
+                        if (!ok) break;
                     } else if (nt == 0 && kt == 0) {
-                        if (elect_one()) mma_commit(bar(BAR_ODONE + t));  // tile without work
+                        // tile without work: its (all-zero) O_t is "final" now, but only after
+                        // the previous unit's O_t was read, which keeps this barrier's phases
+                        // in step with the epilogue that waits on them
+                        if (j > 0 && !wait_bounded(bar(BAR_OFREE + t), (j - 1) & 1, abort_flag, limit)) {
+                            ok = false;
+                            break;
+                        }
+                        if (elect_one()) mma_commit(bar(BAR_ODONE + t));
                         __syncwarp();
                     }
                     if (kt + 1 < nt) {
@@ -447,9 +493,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 ++kv;
             }
-            if (ok && nm == 0) {
-                if (elect_one())
-                    for (int t = 0; t < kTiles; ++t) mma_commit(bar(BAR_ODONE + t));
+            for (int t = 0; ok && nm == 0 && t < kTiles; ++t) {  // unit without any work
+                if (j > 0 && !wait_bounded(bar(BAR_OFREE + t), (j - 1) & 1, abort_flag, limit)) {
+                    ok = false;
+                    break;
+                }
+                if (elect_one()) mma_commit(bar(BAR_ODONE + t));
                 __syncwarp();
             }
         }
@@ -459,8 +508,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             drain_bounded(bar(BAR_MMADONE), 0, limit);
         }
         __syncwarp();
-    } else {
+      }
+    } else if (wg < 2) {
         // =========================== softmax warpgroups =====================
+        regs_inc<kRegsSoftmax>();
         const int t = warp / 4;
         const int wq = warp % 4;
         const int r = wq * 32 + lane;  // row within the tile = TMEM lane
@@ -518,13 +569,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          fmaxf(mx[6], mx[7]));
                 const float m_tile = tmax * sl2;
 
-                // weights 2^(s*scale*log2e - m_use) and their row sum; packed to bf16
-                // pairs and stored as P_t chunk by chunk (32 weights = 16 columns)
-                float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
-                auto weights = [&](float m_use) {
-                    rs0 = rs1 = rs2 = rs3 = 0.f;
+                // raise the running max only when the tile max exceeds it by more than 2^8
+                // (always on the first tile with a visible key: then alpha = 0)
+                float alpha = 1.f;
+                if (m_tile - m_run > kRescaleLog2) {
+                    alpha = ex2_approx(m_run - m_tile);
+                    m_run = m_tile;
+                }
+                const float m_use = m_run == -INFINITY ? 0.f : m_run;
+                // O_t holds P.V of tiles < kt (complete: S_t(kt) was issued after them);
+                // rescale it before this tile's first P.V half may start
+                const bool need = (kt > 0) && (alpha != 1.f);
+                if (__any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+                    for (int c = 0; c < 8; ++c) {
+                        uint32_t o[16];
+                        tmem_ld16(tO + 16 * c, o);
+                        tmem_wait_ld_regs16(o);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
+                        for (int q = 0; q < 16; q += 2) {
+                            float x0, x1;
+                            fmul2_b(x0, x1, __uint_as_float(o[q]), __uint_as_float(o[q + 1]), alpha);
+                            o[q] = __float_as_uint(x0);
+                            o[q + 1] = __float_as_uint(x1);
+                        }
+                        tmem_st16(tO + 16 * c, o);
+                    }
+                }
+                // weights 2^(s*scale*log2e - m_use), their row sum, packed to bf16 pairs and
+                // stored as P_t in two halves of 64 keys (32 columns); each half is handed
+                // to the MMA warp as soon as it is in tensor memory
+                float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                    for (int c = 2 * h; c < 2 * h + 2; ++c) {
                         uint32_t pk[16];
 #pragma unroll
                         for (int q = 0; q < 16; q += 2) {
@@ -548,110 +627,96 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         tmem_st16(tS + 16 * c, pk);
                     }
-                };
-                float alpha = 1.f;
-#if ATTN_SPECULATIVE_EXP
-                // against the running max, known before the tile maximum is reduced
-                // (weights() stores to TMEM warp-collectively: every call is warp-uniform)
-                const bool rise = m_tile - m_run > kRescaleLog2;  // rare after the first tile
-                if (__all_sync(0xffffffffu, m_run == -INFINITY)) {
-                    // first tile of the warp's rows: nothing to speculate on
-                    if (rise) {
-                        alpha = ex2_approx(m_run - m_tile);
-                        m_run = m_tile;
-                    }
-                    weights(m_run == -INFINITY ? 0.f : m_run);
-                } else {
-                    weights(m_run == -INFINITY ? 0.f : m_run);
-                    if (rise) {
-                        alpha = ex2_approx(m_run - m_tile);
-                        m_run = m_tile;
-                    }
-                    if (__any_sync(0xffffffffu, rise)) {
-                        tmem_wait_st();  // the first stores land before they are overwritten
-                        weights(m_run == -INFINITY ? 0.f : m_run);
-                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(bar(BAR_PFULL + 2 * t + h));
                 }
-#else
-                if (m_tile - m_run > kRescaleLog2) {  // the max rose past 2^8 (always on the
-                    alpha = ex2_approx(m_run - m_tile);  // first visible tile: alpha = 0)
-                    m_run = m_tile;
-                }
-                weights(m_run == -INFINITY ? 0.f : m_run);
-#endif
                 l_run = l_run * alpha + ((rs0 + rs1) + (rs2 + rs3));
-                // O_t holds P.V of tiles < kt (complete: S_t(kt) was issued after them)
-                const bool need = (kt > 0) && (alpha != 1.f);
-                if (__any_sync(0xffffffffu, need)) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t o[32];
-                        tmem_ld32(tO + 32 * c, o);
-                        tmem_wait_ld_regs(o);
-#pragma unroll
-                        for (int q = 0; q < 32; q += 2) {
-                            float x0, x1;
-                            fmul2_b(x0, x1, __uint_as_float(o[q]), __uint_as_float(o[q + 1]), alpha);
-                            o[q] = __float_as_uint(x0);
-                            o[q + 1] = __float_as_uint(x1);
-                        }
-                        tmem_st32(tO + 32 * c, o);
-                    }
-                }
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(bar(BAR_PFULL + t));
             }
             if (!ok) break;
 
-            // ------------------------------ epilogue ------------------------------
-            // O_t is final once every P.V of this unit completed
-            const bool got = wait_bounded(bar(BAR_ODONE + t), j & 1, abort_flag, limit);
-            if (!__all_sync(0xffffffffu, got)) {
+            // hand (m, l) of every row to the epilogue warpgroup and start the next unit
+            if (j > 0 && !wait_bounded(bar(BAR_STATSFREE + t), (j - 1) & 1, abort_flag, limit)) {
                 ok = false;
                 break;
             }
-            tc_fence_after();
-            // O_t -> registers 32 columns at a time -> (1/l) -> bf16 -> global (this row's
-            // 256 bytes); the last TMEM load frees O_t for the next unit's first P.V
-            const bool store = row < p.Sq;
-            const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
-            uint4* dst = reinterpret_cast<uint4*>(
-                p.o + ((static_cast<size_t>(w.b) * p.Sq + (store ? row : 0)) * p.Hq + w.hq(t)) * kHeadDim);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t o[32];
-                if (nt > 0) {
-                    tmem_ld32(tO + 32 * c, o);
-                    tmem_wait_ld_regs(o);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = 0u;
+            reinterpret_cast<float2*>(smem + kSmemStats)[t * kBM + r] = make_float2(m_run, l_run);
+            mbar_arrive(bar(BAR_STATSFULL + t));
+        }
+    } else if (wg == 2) {
+        // =========================== epilogue warpgroup =====================
+        regs_dec<kRegsEpilogue>();
+        const int wq = warp % 4;
+        const int r = wq * 32 + lane;  // row within a tile = TMEM lane
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        uint8_t* stage = smem + kSmemStage;
+        bool ok = true;
+        for (int j = 0; ok; ++j) {
+            const int u = unit_of(p, j);
+            if (u < 0) break;
+            const Unit w = decode_unit(p, u);
+            for (int t = 0; t < kTiles; ++t) {
+                // O_t final (every P.V of the unit completed) and (m, l) of its rows
+                const bool got = wait_bounded(bar(BAR_ODONE + t), j & 1, abort_flag, limit) &&
+                                 wait_bounded(bar(BAR_STATSFULL + t), j & 1, abort_flag, limit);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
                 }
-                if (c == 3) {
-                    tc_fence_before();
-                    mbar_arrive(bar(BAR_OFREE + t));
-                }
-                if (store) {
+                tc_fence_after();
+                const float2 ml = reinterpret_cast<const float2*>(smem + kSmemStats)[t * kBM + r];
+                mbar_arrive(bar(BAR_STATSFREE + t));
+                const float m_run = ml.x, l_run = ml.y;
+                const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+                const int nt = w.n(t);
+                const int row = w.row(t) + r;
+                const uint32_t tO = tmem_base + lane_off + kTmemO + 128 * t;
+                const bool tile_in_range = w.row(t) < p.Sq;
+                // two 64-column halves: TMEM -> registers -> (1/l) -> bf16 -> swizzled
+                // staging -> one TMA store each (rows past Sq are clipped by the store)
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t o[64];
+                    if (nt > 0) {
+                        tmem_ld32(tO + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+                        tmem_ld32(tO + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+                        tmem_wait_ld_regs(*reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+                        tmem_wait_ld_regs(*reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 64; ++e) o[e] = 0u;
+                    }
+                    if (h == 1) {  // O_t may now be overwritten by the next unit's first P.V
+                        tc_fence_before();
+                        mbar_arrive(bar(BAR_OFREE + t));
+                    }
+                    if (r == 0) bulk_wait_group_read0();  // the previous store has read the staging
+                    named_bar_sync(1, 128);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {  // 16-byte chunk q of this row's half
                         float f[8];
 #pragma unroll
                         for (int e = 0; e < 8; e += 2)
-                            fmul2_b(f[e], f[e + 1], __uint_as_float(o[8 * q + e]),
-                                    __uint_as_float(o[8 * q + e + 1]), inv_l);
-                        dst[4 * c + q] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
-                                                    pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+                            fmul2_b(f[e], f[e + 1], __uint_as_float(o[8 * q + e]), __uint_as_float(o[8 * q + e + 1]),
+                                    inv_l);
+                        *reinterpret_cast<uint4*>(stage + r * 128 + ((q ^ (r & 7)) * 16)) =
+                            make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                                       pack_bf16x2(f[6], f[7]));
+                    }
+                    fence_proxy_async_smem();
+                    named_bar_sync(1, 128);
+                    if (r == 0 && tile_in_range) {
+                        tma_store_4d(&tm_o, smem_u32(stage), h * 64, w.hq(t), w.row(t), w.b);
+                        bulk_commit_group();
                     }
                 }
-            }
-            if (store) {
-                if (p.lse != nullptr) {
+                if (row < p.Sq && p.lse != nullptr) {
                     const float lse = l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
                     p.lse[(static_cast<size_t>(w.b) * p.Hq + w.hq(t)) * p.Sq + row] = lse;
                 }
             }
         }
+        if (r == 0) bulk_wait_group0();  // every O store has completed before the CTA exits
     }
 
     // ---- teardown: all tensor-memory traffic is complete; free it

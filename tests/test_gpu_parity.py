@@ -40,6 +40,10 @@ SMALL = [
     (1, 1000, 1000, 2, 1, 0, 4.0),      # sharp softmax, running-max rescale
     (2, 640, 640, 4, 4, 1, 4.0),        # sharp + causal
     (1, 96, 4096, 4, 1, 1, 1.0),        # chunked prefill: short query block, long key range
+    # more units than SMs, each with an empty tile: CTAs run several units back to back
+    (1, 300, 77, 160, 160, 1, 1.0),     # row pairs: one tile of every unit sees no key
+    (1, 300, 77, 320, 160, 1, 1.0),     # head pairs: whole units without any key
+    (1, 17, 33, 320, 320, 0, 1.0),      # row pairs: tile 1 of every unit is past Sq
 ]
 
 
