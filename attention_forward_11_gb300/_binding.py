@@ -20,8 +20,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_NAME = "libattn.so"
 
 # Every symbol include/attn.h declares (checked by the CPU tests).
-EXPORTED = ("attn_fwd", "attn_status_str", "attn_check_device_status", "attn_kernel_launches",
-            "attn_debug_wait_timeout")
+EXPORTED = ("attn_fwd", "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_size", "attn_status_str",
+            "attn_check_device_status", "attn_kernel_launches", "attn_debug_wait_timeout")
 
 _lock = threading.Lock()
 _lib = None
@@ -64,6 +64,12 @@ def load_library():
         lib.attn_kernel_launches.restype = ctypes.c_ulonglong
         lib.attn_debug_wait_timeout.argtypes = [ctypes.c_uint, P]
         lib.attn_debug_wait_timeout.restype = I
+        lib.attn_fwd_splitkv_workspace_size.argtypes = [I, I, I, I, I, I, I,
+                                                        ctypes.POINTER(ctypes.c_size_t)]
+        lib.attn_fwd_splitkv_workspace_size.restype = I
+        lib.attn_fwd_splitkv.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, ctypes.c_float, P,
+                                         ctypes.c_size_t, P]
+        lib.attn_fwd_splitkv.restype = I
         _lib = lib
         return lib
 
@@ -99,7 +105,7 @@ def attn_fwd(q, k, v, o=None, lse=None, causal: int = 0, scale: float | None = N
 
     q: bf16 CUDA tensor [B, Sq, Hq, D]; k, v: [B, Skv, Hkv, D]; all contiguous.
     o (optional): bf16 [B, Sq, Hq, D]; lse (optional): fp32 [B, Hq, Sq].
-    causal: 0 none, 1 bottom-right aligned.  Returns (o, lse or None).
+    causal: 0 none, 1 bottom-right aligned, 2 top-left aligned.  Returns (o, lse or None).
     Runs asynchronously on ``stream`` (default: torch's current stream).
     """
     import torch
@@ -123,6 +129,54 @@ def attn_fwd(q, k, v, o=None, lse=None, causal: int = 0, scale: float | None = N
                       int(causal), float(scale), _stream_handle(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd")
+    return o, lse
+
+
+def attn_fwd_splitkv_workspace_size(B: int, Sq: int, Skv: int, Hq: int, Hkv: int, D: int,
+                                    causal: int) -> int:
+    """Workspace bytes attn_fwd_splitkv needs on the current device (0: no split)."""
+    n = ctypes.c_size_t(0)
+    st = int(load_library().attn_fwd_splitkv_workspace_size(B, Sq, Skv, Hq, Hkv, D, causal,
+                                                            ctypes.byref(n)))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_splitkv_workspace_size")
+    return int(n.value)
+
+
+def attn_fwd_splitkv_ptr(q: int, k: int, v: int, o: int, lse: int, B: int, Sq: int, Skv: int,
+                         Hq: int, Hkv: int, D: int, causal: int, scale: float, workspace: int,
+                         workspace_bytes: int, stream: int) -> int:
+    """Raw-pointer call of attn_fwd_splitkv; returns the attn_status_t value."""
+    return int(load_library().attn_fwd_splitkv(q, k, v, o, lse, B, Sq, Skv, Hq, Hkv, D, causal,
+                                               ctypes.c_float(scale), workspace, workspace_bytes,
+                                               stream))
+
+
+def attn_fwd_splitkv(q, k, v, o=None, lse=None, causal: int = 0, scale: float | None = None,
+                     workspace=None, stream=None, want_lse: bool = True):
+    """attn_fwd with KV split across SMs.  `workspace`: a CUDA byte tensor of at
+    least attn_fwd_splitkv_workspace_size(...) bytes, allocated here if None."""
+    import torch
+    B, Sq, Hq, D = q.shape
+    Skv, Hkv = k.shape[1], k.shape[2]
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise AttnError(ATTN_ERR_INVALID_ARG, f"{name} must be a contiguous bf16 CUDA tensor")
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    if scale is None:
+        scale = 1.0 / (D ** 0.5)
+    if workspace is None:
+        n = attn_fwd_splitkv_workspace_size(B, Sq, Skv, Hq, Hkv, D, int(causal))
+        workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
+    st = attn_fwd_splitkv_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                              lse.data_ptr() if lse is not None else 0, B, Sq, Skv, Hq, Hkv, D,
+                              int(causal), float(scale), workspace.data_ptr(), workspace.numel(),
+                              _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_splitkv")
     return o, lse
 
 

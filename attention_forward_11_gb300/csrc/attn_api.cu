@@ -5,11 +5,14 @@
 // tails are handled inside the kernel by TMA zero-fill and key masking.
 #include <attn.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <memory>
 #include <mutex>
+#include <vector>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -57,7 +60,7 @@ bool encode_bshd(CUtensorMap* map, const void* ptr, int B, int S, int H, int D) 
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Per-device one-time set-up: the kernel's shared-memory opt-in and the SM count.
+// Per-device one-time set-up: the kernels' shared-memory opt-in and the SM count.
 bool device_setup(int dev, int* sm_count) {
     static std::mutex mu;
     static int sms[kMaxDevices] = {};
@@ -65,8 +68,10 @@ bool device_setup(int dev, int* sm_count) {
     std::lock_guard<std::mutex> lock(mu);
     if (sms[dev] == 0) {
         int n = 0;
-        if (cudaFuncSetAttribute(attn::fmha_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 attn::kSmemBytes) != cudaSuccess ||
+        if (cudaFuncSetAttribute(attn::fmha_fwd_kernel<attn::PlainSched>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, attn::kSmemBytes) != cudaSuccess ||
+            cudaFuncSetAttribute(attn::fmha_fwd_kernel<attn::SplitSched>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, attn::kSmemBytes) != cudaSuccess ||
             cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
             return false;
         sms[dev] = n;
@@ -80,18 +85,21 @@ bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
     return pa < pb + nb && pb < pa + na;
 }
 
-}  // namespace
-
-extern "C" attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
-                                  int B, int Sq, int Skv, int Hq, int Hkv, int D, int causal,
-                                  float scale, cudaStream_t stream) {
-    // ---- validation: nothing is launched on any error
-    if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+// Size checks shared by every entry point (mirrors the Pallas page's
+// `_attention_forward`): sizes, GQA divisibility, mask mode, scale, head size.
+attn_status_t check_sizes(int B, int Sq, int Skv, int Hq, int Hkv, int D, int causal) {
     if (B < 1 || Sq < 1 || Skv < 1 || Hq < 1 || Hkv < 1 || D < 1) return ATTN_ERR_INVALID_ARG;
     if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
-    if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
-    if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
-    for (const void* ptr : {q, k, v, static_cast<const void*>(o)})
+    if (causal < 0 || causal > 2) return ATTN_ERR_INVALID_ARG;
+    if (D != attn::kHeadDim) return ATTN_ERR_UNSUPPORTED;
+    return ATTN_OK;
+}
+
+// Pointer checks: non-null, 16-byte aligned (TMA), outputs not aliasing inputs.
+attn_status_t check_pointers(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                             int B, int Sq, int Skv, int Hq, int Hkv, int D) {
+    if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+    for (const void* ptr : {q, k, v, o})
         if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return ATTN_ERR_INVALID_ARG;
     if (lse && reinterpret_cast<uintptr_t>(lse) % 4 != 0) return ATTN_ERR_INVALID_ARG;
     const size_t q_bytes = (size_t)B * Sq * Hq * D * 2;
@@ -102,9 +110,13 @@ extern "C" attn_status_t attn_fwd(const void* q, const void* k, const void* v, v
     if (lse && (ranges_overlap(lse, (size_t)B * Hq * Sq * 4, o, q_bytes) ||
                 ranges_overlap(lse, (size_t)B * Hq * Sq * 4, q, q_bytes)))
         return ATTN_ERR_INVALID_ARG;
-    if (D != attn::kHeadDim) return ATTN_ERR_UNSUPPORTED;
+    return ATTN_OK;
+}
 
-    // ---- work decomposition: two 128-row query tiles per CTA sharing one K/V head
+// Work decomposition: two 128-row query tiles per unit sharing one K/V head.
+attn_status_t make_params(int B, int Sq, int Skv, int Hq, int Hkv, int causal, float scale, void* o,
+                          float* lse, attn::FwdParams* out) {
+    if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
     attn::FwdParams p{};
     p.B = B;
     p.Sq = Sq;
@@ -112,6 +124,7 @@ extern "C" attn_status_t attn_fwd(const void* q, const void* k, const void* v, v
     p.Hq = Hq;
     p.Hkv = Hkv;
     p.causal = causal;
+    p.diag = causal == 1 ? Skv - Sq : 0;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     p.lse = lse;
     p.poll_limit = kDefaultPollLimit;
@@ -128,21 +141,194 @@ extern "C" attn_status_t attn_fwd(const void* q, const void* k, const void* v, v
     if (n_units > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
     p.n_units = static_cast<int>(n_units);
     p.o = static_cast<uint16_t*>(o);
+    *out = p;
+    return ATTN_OK;
+}
 
-    CUtensorMap tm_q, tm_k, tm_v, tm_o;
-    if (!encode_bshd(&tm_q, q, B, Sq, Hq, D) || !encode_bshd(&tm_k, k, B, Skv, Hkv, D) ||
-        !encode_bshd(&tm_v, v, B, Skv, Hkv, D) || !encode_bshd(&tm_o, o, B, Sq, Hq, D))
-        return ATTN_ERR_CUDA;
+bool encode_maps(const void* q, const void* k, const void* v, const void* o, int B, int Sq, int Skv, int Hq,
+                 int Hkv, int D, CUtensorMap* tm) {
+    return encode_bshd(&tm[0], q, B, Sq, Hq, D) && encode_bshd(&tm[1], k, B, Skv, Hkv, D) &&
+           encode_bshd(&tm[2], v, B, Skv, Hkv, D) && encode_bshd(&tm[3], o, B, Sq, Hq, D);
+}
 
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || !device_setup(dev, &sms)) return ATTN_ERR_CUDA;
+// ---- split-KV plan: equal contiguous shares of the (unit, KV tile) iterations
+struct SplitPlan {
+    bool split = false;      // false: the whole-unit schedule is used (no workspace)
+    int grid = 0;
+    int n_slots = 0;
+    attn::SplitSched sched{};
+    attn::CombineTable comb{};
+};
+constexpr size_t kWorkspaceAlign = 256;
+
+size_t workspace_bytes_for(int n_slots) {
+    const size_t o_bytes = (size_t)n_slots * attn::kTiles * attn::kBM * attn::kHeadDim * sizeof(float);
+    const size_t ml_bytes = (size_t)n_slots * attn::kTiles * attn::kBM * sizeof(float2);
+    const size_t o_pad = (o_bytes + kWorkspaceAlign - 1) / kWorkspaceAlign * kWorkspaceAlign;
+    return o_pad + ml_bytes;
+}
+
+void build_split_plan(const attn::FwdParams& p, int sms, SplitPlan* plan) {
+    plan->split = false;
+    if (p.n_units < 1 || p.n_units > attn::kMaxPieces) return;
+    std::vector<int> W(p.n_units);
+    long long T = 0;
+    for (int u = 0; u < p.n_units; ++u) {
+        W[u] = attn::decode_unit(p, u).nmax();
+        if (W[u] > 0xFFFF) return;
+        T += W[u];
+    }
+    const int G = static_cast<int>(std::min<long long>(std::min(sms, attn::kMaxSplitCtas), T));
+    if (G < 1) return;
+    std::vector<long long> bnd(G + 1);
+    for (int c = 0; c <= G; ++c) bnd[c] = (long long)c * T / G;
+    attn::SplitSched& sc = plan->sched;
+    attn::CombineTable& cb = plan->comb;
+    std::vector<int> piece_cta;
+    int n_pieces = 0, n_slots = 0, n_comb = 0, c = 0;
+    long long off = 0;
+    auto add = [&](int u, int kb, int ke, int slot, int cta) -> bool {
+        if (n_pieces >= attn::kMaxPieces) return false;
+        sc.piece[n_pieces] = attn::Piece{u, static_cast<unsigned int>(kb) | (static_cast<unsigned int>(ke) << 16),
+                                         slot};
+        piece_cta.push_back(cta);
+        ++n_pieces;
+        return true;
+    };
+    for (int u = 0; u < p.n_units; ++u) {
+        const long long a = off, e = off + W[u];
+        while (c < G - 1 && a >= bnd[c + 1]) ++c;
+        if (W[u] == 0) {  // no KV tile at all: still writes O = 0, LSE = -inf
+            if (!add(u, 0, 0, -1, c)) return;
+            continue;
+        }
+        int c1 = c;
+        while (c1 < G - 1 && e > bnd[c1 + 1]) ++c1;
+        if (c1 == c) {
+            if (!add(u, 0, W[u], -1, c)) return;
+        } else {
+            if (n_comb >= attn::kMaxCombine) return;
+            cb.e[n_comb++] = attn::CombineEntry{u, n_slots, c1 - c + 1};
+            for (int cc = c; cc <= c1; ++cc) {
+                const long long kb = std::max(a, bnd[cc]) - a, ke = std::min(e, bnd[cc + 1]) - a;
+                if (!add(u, static_cast<int>(kb), static_cast<int>(ke), n_slots++, cc)) return;
+            }
+        }
+        off = e;
+    }
+    if (n_comb == 0) return;  // no unit straddles two shares: the whole-unit schedule is as good
+    // first piece of each CTA (pieces are in non-decreasing CTA order)
+    int i = 0;
+    for (int cc = 0; cc <= G; ++cc) {
+        while (i < n_pieces && piece_cta[i] < cc) ++i;
+        sc.cta_begin[cc] = static_cast<unsigned short>(i);
+    }
+    sc.n_pieces = n_pieces;
+    cb.n = n_comb;
+    plan->grid = G;
+    plan->n_slots = n_slots;
+    plan->split = true;
+}
+
+attn_status_t launch_plain(const CUtensorMap* tm, const attn::FwdParams& p, int sms, cudaStream_t stream) {
     // persistent grid: at most one CTA per SM (the CTA holds all 512 TMEM columns)
-    const int grid = static_cast<int>(n_units < sms ? n_units : sms);
-    attn::fmha_fwd_kernel<<<static_cast<unsigned int>(grid), attn::kThreads, attn::kSmemBytes,
-                            stream>>>(tm_q, tm_k, tm_v, tm_o, p);
+    const int grid = p.n_units < sms ? p.n_units : sms;
+    attn::fmha_fwd_kernel<attn::PlainSched><<<static_cast<unsigned int>(grid), attn::kThreads, attn::kSmemBytes,
+                                              stream>>>(tm[0], tm[1], tm[2], tm[3], p, attn::PlainSched{0});
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return ATTN_OK;
+}
+
+attn_status_t launch_split(const CUtensorMap* tm, const attn::FwdParams& p, SplitPlan& plan, void* workspace,
+                           cudaStream_t stream) {
+    const size_t o_bytes = (size_t)plan.n_slots * attn::kTiles * attn::kBM * attn::kHeadDim * sizeof(float);
+    const size_t o_pad = (o_bytes + kWorkspaceAlign - 1) / kWorkspaceAlign * kWorkspaceAlign;
+    plan.sched.ws_o = static_cast<float*>(workspace);
+    plan.sched.ws_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) + o_pad);
+    attn::fmha_fwd_kernel<attn::SplitSched><<<static_cast<unsigned int>(plan.grid), attn::kThreads,
+                                              attn::kSmemBytes, stream>>>(tm[0], tm[1], tm[2], tm[3], p, plan.sched);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    plan.comb.ws_o = plan.sched.ws_o;
+    plan.comb.ws_ml = plan.sched.ws_ml;
+    plan.comb.o = p.o;
+    const long long warps = (long long)plan.comb.n * attn::kTiles * attn::kBM;
+    const unsigned int blocks = static_cast<unsigned int>((warps + attn::kCombineWarps - 1) / attn::kCombineWarps);
+    attn::splitkv_combine_kernel<<<blocks, 32 * attn::kCombineWarps, 0, stream>>>(p, plan.comb);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                                  int B, int Sq, int Skv, int Hq, int Hkv, int D, int causal,
+                                  float scale, cudaStream_t stream) {
+    // ---- validation: nothing is launched on any error
+    if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+    attn_status_t st = check_sizes(B, Sq, Skv, Hq, Hkv, D, causal);
+    if (st == ATTN_ERR_INVALID_ARG) return st;
+    const attn_status_t sp = check_pointers(q, k, v, o, lse, B, Sq, Skv, Hq, Hkv, D > 0 ? D : 1);
+    if (sp != ATTN_OK) return sp;
+    attn::FwdParams p{};
+    const attn_status_t sm = make_params(B, Sq, Skv, Hq, Hkv, causal, scale, o, lse, &p);
+    if (sm != ATTN_OK) return sm;
+    if (st != ATTN_OK) return st;  // valid request, unsupported head size
+    CUtensorMap tm[4];
+    if (!encode_maps(q, k, v, o, B, Sq, Skv, Hq, Hkv, D, tm)) return ATTN_ERR_CUDA;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || !device_setup(dev, &sms)) return ATTN_ERR_CUDA;
+    return launch_plain(tm, p, sms, stream);
+}
+
+extern "C" attn_status_t attn_fwd_splitkv_workspace_size(int B, int Sq, int Skv, int Hq, int Hkv, int D,
+                                                         int causal, size_t* bytes) {
+    if (!bytes) return ATTN_ERR_INVALID_ARG;
+    *bytes = 0;
+    const attn_status_t st = check_sizes(B, Sq, Skv, Hq, Hkv, D, causal);
+    if (st != ATTN_OK) return st;
+    attn::FwdParams p{};
+    const attn_status_t sm = make_params(B, Sq, Skv, Hq, Hkv, causal, 1.0f, nullptr, nullptr, &p);
+    if (sm != ATTN_OK) return sm;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || !device_setup(dev, &sms)) return ATTN_ERR_CUDA;
+    std::unique_ptr<SplitPlan> plan(new SplitPlan());
+    build_split_plan(p, sms, plan.get());
+    *bytes = plan->split ? workspace_bytes_for(plan->n_slots) : 0;
+    return ATTN_OK;
+}
+
+extern "C" attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                                          int Sq, int Skv, int Hq, int Hkv, int D, int causal, float scale,
+                                          void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+    attn_status_t st = check_sizes(B, Sq, Skv, Hq, Hkv, D, causal);
+    if (st == ATTN_ERR_INVALID_ARG) return st;
+    const attn_status_t sp = check_pointers(q, k, v, o, lse, B, Sq, Skv, Hq, Hkv, D > 0 ? D : 1);
+    if (sp != ATTN_OK) return sp;
+    if (workspace && reinterpret_cast<uintptr_t>(workspace) % kWorkspaceAlign != 0) return ATTN_ERR_INVALID_ARG;
+    attn::FwdParams p{};
+    const attn_status_t sm = make_params(B, Sq, Skv, Hq, Hkv, causal, scale, o, lse, &p);
+    if (sm != ATTN_OK) return sm;
+    if (st != ATTN_OK) return st;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || !device_setup(dev, &sms)) return ATTN_ERR_CUDA;
+    std::unique_ptr<SplitPlan> plan(new SplitPlan());
+    build_split_plan(p, sms, plan.get());
+    if (plan->split) {
+        const size_t need = workspace_bytes_for(plan->n_slots);
+        if (!workspace || workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
+        const size_t q_bytes = (size_t)B * Sq * Hq * D * 2, kv_bytes = (size_t)B * Skv * Hkv * D * 2;
+        if (ranges_overlap(workspace, need, q, q_bytes) || ranges_overlap(workspace, need, k, kv_bytes) ||
+            ranges_overlap(workspace, need, v, kv_bytes) || ranges_overlap(workspace, need, o, q_bytes) ||
+            (lse && ranges_overlap(workspace, need, lse, (size_t)B * Hq * Sq * 4)))
+            return ATTN_ERR_INVALID_ARG;
+    }
+    CUtensorMap tm[4];
+    if (!encode_maps(q, k, v, o, B, Sq, Skv, Hq, Hkv, D, tm)) return ATTN_ERR_CUDA;
+    return plan->split ? launch_split(tm, p, *plan, workspace, stream) : launch_plain(tm, p, sms, stream);
 }
 
 extern "C" const char* attn_status_str(attn_status_t status) {

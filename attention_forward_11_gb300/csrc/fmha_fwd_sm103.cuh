@@ -38,9 +38,9 @@
 // The weights of a tile are handed to the MMA warp in two halves of 64 keys, so
 // the first half of O += P.V runs while the second half's exponentials are made.
 //
-// Causal (bottom-right aligned: key j visible from row i iff j <= i + Skv - Sq):
-// KV tiles entirely above a tile's last visible key are never loaded or
-// multiplied; the element mask is applied only on the tiles that cross the
+// Causal masks (bottom-right aligned: key j visible from row i iff j <= i + Skv - Sq;
+// top-left aligned: iff j <= i): KV tiles entirely above a tile's last visible key
+// are never loaded or multiplied; the element mask is applied only on the tiles that cross the
 // diagonal or the ragged key tail.
 //
 // Every mbarrier wait is bounded: when a wait runs out, the thread records
@@ -49,6 +49,7 @@
 // bounded waits, and tensor memory is freed before the CTA exits.
 #pragma once
 #include <cstdint>
+#include <type_traits>
 #include <cuda.h>
 
 #include "sm103_ptx.cuh"
@@ -119,7 +120,8 @@ __device__ unsigned int g_attn_status = 0;
 
 struct FwdParams {
     int B, Sq, Skv, Hq, Hkv;
-    int causal;             // 0 or 1 (bottom-right)
+    int causal;             // 0: none; 1: bottom-right; 2: top-left
+    int diag;               // key j visible from row i iff j <= i + diag (when causal)
     float scale_log2;       // softmax scale * log2(e)
     uint16_t* o;            // [B, Sq, Hq, D] bf16
     float* lse;             // [B, Hq, Sq] fp32, or nullptr
@@ -175,30 +177,32 @@ __device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[32]) {
 }
 
 // Number of KV tiles a query tile [row0, row0 + 128) must visit.
-__device__ __forceinline__ int kv_tiles_for(const FwdParams& p, int row0) {
+__host__ __device__ __forceinline__ int kv_tiles_for(const FwdParams& p, int row0) {
     if (row0 >= p.Sq) return 0;
     const int n_all = (p.Skv + kBN - 1) / kBN;
     if (!p.causal) return n_all;
-    const int last_row = min(row0 + kBM - 1, p.Sq - 1);
-    const long long last_key = (long long)last_row + (p.Skv - p.Sq);
+    const int last_row = row0 + kBM - 1 < p.Sq - 1 ? row0 + kBM - 1 : p.Sq - 1;
+    const long long last_key = (long long)last_row + p.diag;
     if (last_key < 0) return 0;
     const long long n = last_key / kBN + 1;
     return n < n_all ? (int)n : n_all;
 }
 
-// Decoded work unit.
+// Decoded work item: a unit, or (split-KV) the KV tiles [kb, kb + nmax) of a unit.
 struct Unit {
     int b, hkv;
     int hq0, hq1;      // query heads of tile 0 / tile 1
     int row0, row1;    // first query row of tile 0 / tile 1
-    int n0, n1;        // KV tiles each tile visits
-    __device__ __forceinline__ int hq(int t) const { return t ? hq1 : hq0; }
-    __device__ __forceinline__ int row(int t) const { return t ? row1 : row0; }
-    __device__ __forceinline__ int n(int t) const { return t ? n1 : n0; }
-    __device__ __forceinline__ int nmax() const { return n0 > n1 ? n0 : n1; }
+    int n0, n1;        // KV tiles each tile visits in this item (from kb on)
+    int kb;            // first KV tile of the item
+    int slot;          // split-KV: workspace slot of a partial item; -1: final output
+    __host__ __device__ __forceinline__ int hq(int t) const { return t ? hq1 : hq0; }
+    __host__ __device__ __forceinline__ int row(int t) const { return t ? row1 : row0; }
+    __host__ __device__ __forceinline__ int n(int t) const { return t ? n1 : n0; }
+    __host__ __device__ __forceinline__ int nmax() const { return n0 > n1 ? n0 : n1; }
 };
 
-__device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
+__host__ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
     Unit w;
     const int inner_count = p.B * p.n_head_units;
     const int ru = u / inner_count;
@@ -218,6 +222,8 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
     w.hkv = w.hq0 / (p.Hq / p.Hkv);
     w.n0 = kv_tiles_for(p, w.row0);
     w.n1 = kv_tiles_for(p, w.row1);
+    w.kb = 0;
+    w.slot = -1;
     return w;
 }
 
@@ -229,10 +235,56 @@ __device__ __forceinline__ int unit_of(const FwdParams& p, int j) {
     return u < p.n_units ? static_cast<int>(u) : -1;
 }
 
+// ---- schedules of work items over the persistent grid
+// Whole units, longest first, in the snake order of unit_of().
+struct PlainSched {
+    int unused;
+};
+
+// Split-KV: the host cuts the sequence of (unit, KV tile) iterations into equal
+// contiguous shares, one per CTA.  A unit that straddles shares becomes several
+// pieces; each writes its raw fp32 accumulator and (m, l) to a workspace slot and
+// the combine kernel merges them.  Units inside one share write O directly.
+struct Piece {
+    int unit;
+    unsigned int krange;  // first KV tile | (end KV tile << 16)
+    int slot;             // workspace slot, or -1 for a whole unit
+};
+constexpr int kMaxPieces = 1024;
+constexpr int kMaxSplitCtas = 256;
+struct SplitSched {
+    float* ws_o;          // [slot][tile][row][D] fp32 raw accumulators
+    float2* ws_ml;        // [slot][tile][row] (running max in log2 units, row sum)
+    int n_pieces;
+    unsigned short cta_begin[kMaxSplitCtas + 1];
+    Piece piece[kMaxPieces];
+};
+
+__device__ __forceinline__ bool get_work(const FwdParams& p, const PlainSched&, int j, Unit& w) {
+    const int u = unit_of(p, j);
+    if (u < 0) return false;
+    w = decode_unit(p, u);
+    return true;
+}
+
+__device__ __forceinline__ bool get_work(const FwdParams& p, const SplitSched& sc, int j, Unit& w) {
+    const int i = sc.cta_begin[blockIdx.x] + j;
+    if (i >= sc.cta_begin[blockIdx.x + 1]) return false;
+    const Piece pc = sc.piece[i];
+    w = decode_unit(p, pc.unit);
+    const int kb = static_cast<int>(pc.krange & 0xFFFFu), ke = static_cast<int>(pc.krange >> 16);
+    w.n0 = max(0, min(w.n0, ke) - kb);
+    w.n1 = max(0, min(w.n1, ke) - kb);
+    w.kb = kb;
+    w.slot = pc.slot;
+    return true;
+}
+
+template <class Sched>
 __global__ void __launch_bounds__(kThreads, 1)
     fmha_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                    const FwdParams p) {
+                    const FwdParams p, const __grid_constant__ Sched sched) {
     extern __shared__ uint8_t smem_raw[];
     // align in the shared window (swizzle atoms and TMA boxes want 1024 bytes)
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -294,9 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             int q_issued[kTiles] = {0, 0};   // Q_t fills issued so far
             bool ok = true;
             for (int j = 0; ok; ++j) {
-                const int u = unit_of(p, j);
-                if (u < 0) break;
-                const Unit w = decode_unit(p, u);
+                Unit w;
+                if (!get_work(p, sched, j, w)) break;
                 for (int t = 0; t < kTiles; ++t) {
                     // Q_t of the previous unit must be consumed by its last S_t MMA
                     if (j > 0 && !wait_bounded(bar(BAR_QEMPTY + t), (j - 1) & 1, abort_flag, limit)) {
@@ -310,9 +361,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++q_issued[t];
                 }
                 if (!ok) break;
-                const int un = unit_of(p, j + 1);
-                if (un >= 0) {  // warm L2 with the next unit's Q while this unit runs
-                    const Unit wn = decode_unit(p, un);
+                Unit wn;
+                if (get_work(p, sched, j + 1, wn)) {  // warm L2 with the next unit's Q meanwhile
                     for (int t = 0; t < kTiles; ++t)
                         for (int h = 0; h < 2; ++h) tma_prefetch_l2_4d(&tm_q, h * 64, wn.hq(t), wn.row(t), wn.b);
                 }
@@ -326,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(bar(BAR_KFULL + ks), kTileBytes);
                     for (int h = 0; h < 2; ++h)
                         tma_load_4d(sbase + kSmemK + ks * kTileBytes + h * kHalfBytes, &tm_k, h * 64,
-                                    w.hkv, kt * kBN, w.b, bar(BAR_KFULL + ks), pol_kv);
+                                    w.hkv, (w.kb + kt) * kBN, w.b, bar(BAR_KFULL + ks), pol_kv);
                     ++k_issued;
                     const int vs = v_issued % kVStages, vuse = v_issued / kVStages;
                     if (vuse > 0 && !wait_bounded(bar(BAR_VEMPTY + vs), (vuse - 1) & 1, abort_flag, limit)) {
@@ -336,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(bar(BAR_VFULL + vs), kTileBytes);
                     for (int h = 0; h < 2; ++h)
                         tma_load_4d(sbase + kSmemV + vs * kTileBytes + h * kHalfBytes, &tm_v, h * 64,
-                                    w.hkv, kt * kBN, w.b, bar(BAR_VFULL + vs), pol_kv);
+                                    w.hkv, (w.kb + kt) * kBN, w.b, bar(BAR_VFULL + vs), pol_kv);
                     ++v_issued;
                 }
             }
@@ -389,9 +439,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int sc0 = 0, sc1 = 0;       // S_t products issued so far (s_full / p_full phase)
         bool ok = true;
         for (int j = 0; ok; ++j) {
-            const int u = unit_of(p, j);
-            if (u < 0) break;
-            const Unit w = decode_unit(p, u);
+            Unit w;
+            if (!get_work(p, sched, j, w)) break;
             const int nm = w.nmax();
             // S_t(0) for each tile that has work; Q_t must have landed
             bool k_ready = false;
@@ -523,12 +572,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
 
         for (int j = 0; ok; ++j) {
-            const int u = unit_of(p, j);
-            if (u < 0) break;
-            const Unit w = decode_unit(p, u);
+            Unit w;
+            if (!get_work(p, sched, j, w)) break;
             const int nt = w.n(t);
             const int row = w.row(t) + r;
-            const long long lim_ll = p.causal ? min((long long)row + (p.Skv - p.Sq), (long long)p.Skv - 1)
+            const long long lim_ll = p.causal ? min((long long)row + p.diag, (long long)p.Skv - 1)
                                               : (long long)p.Skv - 1;
             const int lim = static_cast<int>(lim_ll < -1 ? -1 : lim_ll);  // last visible key
             float m_run = -INFINITY;  // running max (log2 units of scaled logits) used by the weights
@@ -549,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < 4; ++c) tmem_wait_ld_regs(*reinterpret_cast<uint32_t(*)[32]>(&s[32 * c]));
 
-                const int nvis = lim - kt * kBN + 1;  // visible keys of this row in the tile
+                const int nvis = lim - (w.kb + kt) * kBN + 1;  // visible keys of this row in the tile
                 if (nvis < kBN) {
 #pragma unroll
                     for (int jj = 0; jj < kBN; ++jj)
@@ -652,9 +700,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* stage = smem + kSmemStage;
         bool ok = true;
         for (int j = 0; ok; ++j) {
-            const int u = unit_of(p, j);
-            if (u < 0) break;
-            const Unit w = decode_unit(p, u);
+            Unit w;
+            if (!get_work(p, sched, j, w)) break;
             for (int t = 0; t < kTiles; ++t) {
                 // O_t final (every P.V of the unit completed) and (m, l) of its rows
                 const bool got = wait_bounded(bar(BAR_ODONE + t), j & 1, abort_flag, limit) &&
@@ -672,6 +719,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int row = w.row(t) + r;
                 const uint32_t tO = tmem_base + lane_off + kTmemO + 128 * t;
                 const bool tile_in_range = w.row(t) < p.Sq;
+                if constexpr (std::is_same<Sched, SplitSched>::value) {
+                    if (w.slot >= 0) {
+                        // a piece of a split unit: the raw fp32 accumulator and (m, l) of
+                        // every row go to its workspace slot for the combine kernel
+                        const size_t rr = (static_cast<size_t>(w.slot) * kTiles + t) * kBM + r;
+                        uint4* dst = reinterpret_cast<uint4*>(sched.ws_o + rr * kHeadDim);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            uint32_t o[64];
+                            if (nt > 0) {
+                                tmem_ld32(tO + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+                                tmem_ld32(tO + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+                                tmem_wait_ld_regs(*reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+                                tmem_wait_ld_regs(*reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 64; ++e) o[e] = 0u;
+                            }
+                            if (h == 1) {  // O_t may now be overwritten by the next item's first P.V
+                                tc_fence_before();
+                                mbar_arrive(bar(BAR_OFREE + t));
+                            }
+#pragma unroll
+                            for (int q = 0; q < 16; ++q)
+                                dst[16 * h + q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+                        }
+                        sched.ws_ml[rr] = make_float2(m_run, l_run);
+                        continue;
+                    }
+                }
                 // two 64-column halves: TMEM -> registers -> (1/l) -> bf16 -> swizzled
                 // staging -> one TMA store each (rows past Sq are clipped by the store)
 #pragma unroll
@@ -726,6 +803,68 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem_base, kTmemCols);
     }
+}
+
+// ---- split-KV combine
+// Merges the partial (m, l, O) of the pieces of each split unit -- the rule of the
+// kernbench page's `_merge_running`, in log2 units:
+//   M = max_s m_s,  L = sum_s l_s 2^(m_s - M),  O = sum_s O_s 2^(m_s - M) / L,
+//   LSE = (M + log2 L) ln 2;  a row no piece saw a key of gets O = 0, LSE = -inf.
+// One warp per (split unit, tile, row); lane i owns columns 4i .. 4i+3.
+struct CombineEntry {
+    int unit;
+    int first_slot;
+    int n_slots;
+};
+constexpr int kMaxCombine = 512;
+constexpr int kCombineWarps = 8;
+struct CombineTable {
+    const float* ws_o;
+    const float2* ws_ml;
+    uint16_t* o;          // [B, Sq, Hq, D] bf16
+    int n;
+    CombineEntry e[kMaxCombine];
+};
+
+__global__ void __launch_bounds__(32 * kCombineWarps)
+    splitkv_combine_kernel(const FwdParams p, const __grid_constant__ CombineTable ct) {
+    const int gw = static_cast<int>(blockIdx.x) * kCombineWarps + static_cast<int>(threadIdx.x) / 32;
+    const int lane = static_cast<int>(threadIdx.x) & 31;
+    const int entry = gw / (kTiles * kBM);
+    if (entry >= ct.n) return;
+    const int t = (gw / kBM) % kTiles;
+    const int r = gw % kBM;
+    const CombineEntry e = ct.e[entry];
+    const Unit w = decode_unit(p, e.unit);
+    const int row = w.row(t) + r;
+    if (row >= p.Sq) return;
+    float M = -INFINITY;
+    for (int sl = 0; sl < e.n_slots; ++sl) {
+        const float2 ml = ct.ws_ml[((static_cast<size_t>(e.first_slot) + sl) * kTiles + t) * kBM + r];
+        if (ml.y > 0.f) M = fmaxf(M, ml.x);
+    }
+    float L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sl = 0; sl < e.n_slots; ++sl) {
+        const size_t rr = ((static_cast<size_t>(e.first_slot) + sl) * kTiles + t) * kBM + r;
+        const float2 ml = ct.ws_ml[rr];
+        if (!(ml.y > 0.f)) continue;  // this piece saw no key of the row
+        const float a = exp2f(ml.x - M);
+        const float4 v = reinterpret_cast<const float4*>(ct.ws_o + rr * kHeadDim)[lane];
+        L += ml.y * a;
+        acc.x += v.x * a;
+        acc.y += v.y * a;
+        acc.z += v.z * a;
+        acc.w += v.w * a;
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    uint2 out;
+    out.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+    out.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+    reinterpret_cast<uint2*>(ct.o + ((static_cast<size_t>(w.b) * p.Sq + row) * p.Hq + w.hq(t)) * kHeadDim)[lane] = out;
+    if (lane == 0 && p.lse != nullptr)
+        p.lse[(static_cast<size_t>(w.b) * p.Hq + w.hq(t)) * p.Sq + row] =
+            L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
 }
 
 // Failure-detection self-test: one thread waits on an mbarrier that nothing

@@ -47,7 +47,7 @@ def visible_pairs(w) -> int:
     """Exact number of (query row, key) pairs the mask lets through, per head and batch."""
     if not w.causal:
         return w.Sq * w.Skv
-    off = w.Skv - w.Sq
+    off = w.Skv - w.Sq if w.causal == 1 else 0
     total = 0
     for i in range(w.Sq):
         total += max(0, min(w.Skv, i + off + 1))
@@ -169,7 +169,7 @@ def oracle_sample_rate(w, target_s: float, seed: int = 0, q=None, k=None, v=None
                          rng.integers(0, w.Sq, n)], axis=1).astype(np.int64)
 
     def flops_of(rows):
-        off = w.Skv - w.Sq
+        off = w.Skv - w.Sq if w.causal == 1 else 0
         vis = np.minimum(w.Skv, rows[:, 2] + off + 1) if w.causal else np.full(len(rows), w.Skv)
         return float(4 * w.D * np.maximum(vis, 0).sum())
 
@@ -177,7 +177,7 @@ def oracle_sample_rate(w, target_s: float, seed: int = 0, q=None, k=None, v=None
     n, dt = 64, 0.0
     while True:
         t0 = time.perf_counter()
-        oracle.attn_rows(q, k, v, rows_of(n), bool(w.causal), w.scale)
+        oracle.attn_rows(q, k, v, rows_of(n), int(w.causal), w.scale)
         dt = time.perf_counter() - t0
         if dt >= target_s / 8 or n >= 1_000_000:
             break
@@ -185,7 +185,7 @@ def oracle_sample_rate(w, target_s: float, seed: int = 0, q=None, k=None, v=None
     n = int(max(64, min(4_000_000, n * target_s / max(dt, 1e-4))))
     rows = rows_of(n)
     t0 = time.perf_counter()
-    oracle.attn_rows(q, k, v, rows, bool(w.causal), w.scale)
+    oracle.attn_rows(q, k, v, rows, int(w.causal), w.scale)
     dt = time.perf_counter() - t0
     return flops_of(rows) / dt / 1e12, dt, n, oracle.num_threads()
 
@@ -286,11 +286,20 @@ def run_ours(args, w):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
+    ws_bytes = 0
+    if args.path == "splitkv":  # the caller's scratch, allocated once outside the timed region
+        ws_bytes = fa.attn_fwd_splitkv_workspace_size(w.B, w.Sq, w.Skv, w.Hq, w.Hkv, w.D, w.causal)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
 
     def step():
-        st = fa.attn_fwd_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                             lse.data_ptr(), w.B, w.Sq, w.Skv, w.Hq, w.Hkv, w.D, w.causal,
-                             w.scale, sh)
+        if args.path == "splitkv":
+            st = fa.attn_fwd_splitkv_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                         lse.data_ptr(), w.B, w.Sq, w.Skv, w.Hq, w.Hkv, w.D,
+                                         w.causal, w.scale, ws.data_ptr(), ws_bytes, sh)
+        else:
+            st = fa.attn_fwd_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                 lse.data_ptr(), w.B, w.Sq, w.Skv, w.Hq, w.Hkv, w.D, w.causal,
+                                 w.scale, sh)
         if st != fa.ATTN_OK:
             raise fa.AttnError(st, "attn_fwd")
 
@@ -364,6 +373,8 @@ def run_ours(args, w):
         "warmup": args.warmup, "ms_per_step": 1e3 * mean_launch_s, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {**w.as_dict(), "parallelism": "replicas" if world > 1 else "single",
+                   "entry_point": "attn_fwd_splitkv" if args.path == "splitkv" else "attn_fwd",
+                   "workspace_bytes": ws_bytes,
                    "l2": "flushed between steps (256 MiB write); inputs also exceed L2",
                    "metric_flops_per_step": flops, "exact_visible_pair_flops_per_step": exact,
                    "pct_of_peak": 100.0 * value / peak},
@@ -399,6 +410,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", choices=["fwd", "splitkv"], default="fwd",
+                    help="entry point timed: attn_fwd, or attn_fwd_splitkv with its workspace")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     w = inputs.WORKLOADS[args.workload]

@@ -17,11 +17,13 @@
  * tutorial's non-persistent FA kernel, on Blackwell tensor cores (tcgen05).
  *
  * Plain pointers and sizes only; no framework types.  All functions are
- * thread-safe.  The library allocates no device memory.
+ * thread-safe.  The library allocates no device memory: scratch memory, where a
+ * path needs some, is passed in by the caller.
  */
 #ifndef LIBATTN_ATTN_H_
 #define LIBATTN_ATTN_H_
 
+#include <stddef.h>
 #include <cuda_runtime_api.h>
 
 #ifdef __cplusplus
@@ -46,9 +48,10 @@ typedef enum {
  * B, Sq, Skv, Hq, Hkv, D  sizes; every one >= 1, Hq a multiple of Hkv, D == 128.
  *      Sq and Skv may be any length (ragged tails are handled in the kernel).
  * causal 0: every key visible.  1: key j visible from query i iff
- *      j <= i + (Skv - Sq) (bottom-right aligned; the top-left rule of the
- *      Pallas page when Sq == Skv).  A query row that sees no key gets O = 0
- *      and LSE = -inf.
+ *      j <= i + (Skv - Sq) (bottom-right aligned, as in chunked prefill).
+ *      2: iff j <= i (top-left aligned, the Pallas page's reference mask).
+ *      1 and 2 coincide when Sq == Skv.  A query row that sees no key gets
+ *      O = 0 and LSE = -inf.
  * scale  finite, > 0 (typically 1/sqrt(D)).
  * stream CUDA stream the kernel runs on (0 = legacy default stream).
  *
@@ -61,6 +64,32 @@ typedef enum {
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                        int Sq, int Skv, int Hq, int Hkv, int D, int causal, float scale,
                        cudaStream_t stream);
+
+/*
+ * Split-KV forward for problems with too few query tiles to fill the GPU
+ * (short query blocks against long key ranges, e.g. chunked prefill).  The
+ * same operation and arguments as attn_fwd, plus a device workspace the caller
+ * allocates.  This is the single-GPU form of the kernbench page's group
+ * sequence parallelism (`_gqa_attention_prefill_short.py`): the iterations over
+ * (query tile pair, KV tile) are cut into equal contiguous shares, one per SM; a
+ * tile pair whose KV range straddles shares is computed in pieces whose partial
+ * (m, l, O) are merged by that page's `_merge_running` rule in a second kernel.
+ *
+ * attn_fwd_splitkv_workspace_size: bytes of workspace attn_fwd_splitkv needs
+ *   for this problem on the current device (it depends on the SM count); 0 when
+ *   no split pays off, and then attn_fwd_splitkv runs exactly what attn_fwd runs.
+ * attn_fwd_splitkv: workspace device pointer (256-byte aligned, not aliasing
+ *   any other argument) of at least that many bytes, or NULL when the size is 0.
+ *   The workspace is scratch: its contents are undefined before and after the
+ *   call, and two calls that overlap in time on the GPU must not share one.
+ *   Errors as attn_fwd; ATTN_ERR_INVALID_ARG also for a missing or short workspace.
+ */
+attn_status_t attn_fwd_splitkv_workspace_size(int B, int Sq, int Skv, int Hq, int Hkv, int D,
+                                              int causal, size_t* bytes);
+attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                               int B, int Sq, int Skv, int Hq, int Hkv, int D, int causal,
+                               float scale, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream);
 
 /* Static, human-readable name of a status code (never NULL). */
 const char* attn_status_str(attn_status_t status);

@@ -96,27 +96,28 @@ def num_threads() -> int:
     return int(_load().oracle_num_threads())
 
 
-def attn_rows(q, k, v, rows, causal: bool, scale: float):
-    """fp64 o (len(rows) x D) and lse (len(rows)) for the listed (b, h, i) rows."""
+def attn_rows(q, k, v, rows, causal: int, scale: float):
+    """fp64 o (len(rows) x D) and lse (len(rows)) for the listed (b, h, i) rows.
+    causal: 0 none, 1 bottom-right (j <= i + Skv - Sq), 2 top-left (j <= i)."""
     B, Sq, Skv, Hq, Hkv, D = _check_inputs(q, k, v)
     rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
     o = np.zeros((rows.shape[0], D), dtype=np.float64)
     lse = np.zeros(rows.shape[0], dtype=np.float64)
     rc = _load().oracle_attn_rows(_ptr(q), _ptr(k), _ptr(v), B, Sq, Skv, Hq, Hkv, D,
-                                  int(bool(causal)), float(scale), rows.shape[0],
+                                  int(causal), float(scale), rows.shape[0],
                                   _ptr(rows), _ptr(o), _ptr(lse))
     if rc != 0:
         raise ValueError("oracle_attn_rows rejected its arguments")
     return o, lse
 
 
-def attn_full(q, k, v, causal: bool, scale: float):
+def attn_full(q, k, v, causal: int, scale: float):
     """fp64 o [B,Sq,Hq,D] and lse [B,Hq,Sq] for every row."""
     B, Sq, Skv, Hq, Hkv, D = _check_inputs(q, k, v)
     o = np.zeros((B, Sq, Hq, D), dtype=np.float64)
     lse = np.zeros((B, Hq, Sq), dtype=np.float64)
     rc = _load().oracle_attn_fwd(_ptr(q), _ptr(k), _ptr(v), B, Sq, Skv, Hq, Hkv, D,
-                                 int(bool(causal)), float(scale), _ptr(o), _ptr(lse))
+                                 int(causal), float(scale), _ptr(o), _ptr(lse))
     if rc != 0:
         raise ValueError("oracle_attn_fwd rejected its arguments")
     return o, lse
@@ -130,7 +131,7 @@ def partial_triple(q, k, v, causal: bool, scale: float, b: int, h: int, i: int,
     l = np.zeros(1, dtype=np.float64)
     o = np.zeros(D, dtype=np.float64)
     rc = _load().oracle_partial_triple(_ptr(q), _ptr(k), _ptr(v), B, Sq, Skv, Hq, Hkv, D,
-                                       int(bool(causal)), float(scale), b, h, i, j_lo, j_hi,
+                                       int(causal), float(scale), b, h, i, j_lo, j_hi,
                                        _ptr(m), _ptr(l), _ptr(o))
     if rc != 0:
         raise ValueError("oracle_partial_triple rejected its arguments")

@@ -17,10 +17,11 @@
  * divide by the row sum) written out in fp64, with the caller's scale applied
  * to the logits and a natural-log LSE.
  *
- * Visibility: without a mask every key 0..Skv-1 is visible.  With causal=1 the
- * mask is bottom-right aligned: key j is visible from query i iff
- * j <= i + (Skv - Sq).  For Sq == Skv this is the top-left rule of the Pallas
- * page's reference (`mask = q_idx >= kv_idx`).
+ * Visibility: without a mask (causal=0) every key 0..Skv-1 is visible.  With
+ * causal=1 the mask is bottom-right aligned: key j is visible from query i iff
+ * j <= i + (Skv - Sq).  With causal=2 it is top-left aligned: j <= i, the rule of
+ * the Pallas page's reference (`mask = q_idx >= kv_idx`); the two coincide when
+ * Sq == Skv.
  * A row with no visible key gets o = 0 and lse = -inf (the pages leave this
  * case open; this is the reading the tests and the GPU path share).
  *
@@ -56,8 +57,8 @@ typedef struct {
 
 /* last visible key index + 1 for query row i (may be <= 0: no visible key) */
 static long visible_end(const problem_t *p, long i) {
-    if (!p->causal) return p->Skv;
-    long end = i + (p->Skv - p->Sq) + 1;
+    if (p->causal == 0) return p->Skv;
+    long end = (p->causal == 1) ? i + (p->Skv - p->Sq) + 1 : i + 1;
     return end < p->Skv ? end : p->Skv;
 }
 
@@ -115,8 +116,8 @@ static int check_dims(long B, long Sq, long Skv, long Hq, long Hkv, long D) {
 int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, long B, long Sq,
                      long Skv, long Hq, long Hkv, long D, int causal, double scale, long nrows,
                      const long *rows, double *o_out, double *lse_out) {
-    if (check_dims(B, Sq, Skv, Hq, Hkv, D)) return -1;
-    problem_t p = {q, k, v, B, Sq, Skv, Hq, Hkv, D, causal != 0, scale};
+    if (check_dims(B, Sq, Skv, Hq, Hkv, D) || causal < 0 || causal > 2) return -1;
+    problem_t p = {q, k, v, B, Sq, Skv, Hq, Hkv, D, causal, scale};
     for (long r = 0; r < nrows; ++r) {
         const long *t = rows + 3 * r;
         if (t[0] < 0 || t[0] >= B || t[1] < 0 || t[1] >= Hq || t[2] < 0 || t[2] >= Sq)
@@ -157,8 +158,8 @@ int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, lo
 int oracle_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, long B, long Sq,
                     long Skv, long Hq, long Hkv, long D, int causal, double scale,
                     double *o_out, double *lse_out) {
-    if (check_dims(B, Sq, Skv, Hq, Hkv, D)) return -1;
-    problem_t p = {q, k, v, B, Sq, Skv, Hq, Hkv, D, causal != 0, scale};
+    if (check_dims(B, Sq, Skv, Hq, Hkv, D) || causal < 0 || causal > 2) return -1;
+    problem_t p = {q, k, v, B, Sq, Skv, Hq, Hkv, D, causal, scale};
     const long nrows = B * Hq * Sq;
     int bad = 0;
 #pragma omp parallel
@@ -198,10 +199,10 @@ int oracle_partial_triple(const uint16_t *q, const uint16_t *k, const uint16_t *
                           long Sq, long Skv, long Hq, long Hkv, long D, int causal,
                           double scale, long b, long h, long i, long j_lo, long j_hi,
                           double *m_out, double *l_out, double *o_out) {
-    if (check_dims(B, Sq, Skv, Hq, Hkv, D)) return -1;
+    if (check_dims(B, Sq, Skv, Hq, Hkv, D) || causal < 0 || causal > 2) return -1;
     if (b < 0 || b >= B || h < 0 || h >= Hq || i < 0 || i >= Sq) return -1;
     if (j_lo < 0 || j_hi > Skv || j_lo > j_hi) return -1;
-    problem_t p = {q, k, v, B, Sq, Skv, Hq, Hkv, D, causal != 0, scale};
+    problem_t p = {q, k, v, B, Sq, Skv, Hq, Hkv, D, causal, scale};
     double *s_buf = (double *)malloc(sizeof(double) * (size_t)(j_hi - j_lo + 1));
     double *qd = (double *)malloc(sizeof(double) * (size_t)D);
     int rc = 0;

@@ -5,7 +5,8 @@ shares no code with it.  Written per head with a dense masked logit matrix
 (one numpy matmul per head), a masked row maximum, exponentials, row sums and
 a second matmul with V -- the Pallas page's ``attention_reference`` (fp32
 einsum, ``logits.max``, ``exp``, divide by the row sum) in fp64 with the
-caller's scale, a bottom-right causal mask and a natural-log LSE.
+caller's scale, a bottom-right (causal=1) or top-left (causal=2) mask and a
+natural-log LSE.
 """
 from __future__ import annotations
 
@@ -17,7 +18,7 @@ def _widen(bits):
         np.float64)
 
 
-def attention(q_bits, k_bits, v_bits, causal: bool, scale: float):
+def attention(q_bits, k_bits, v_bits, causal: int, scale: float):
     """Returns (o [B,Sq,Hq,D] fp64, lse [B,Hq,Sq] fp64)."""
     q, k, v = _widen(q_bits), _widen(k_bits), _widen(v_bits)
     B, Sq, Hq, D = q.shape
@@ -27,7 +28,12 @@ def attention(q_bits, k_bits, v_bits, causal: bool, scale: float):
     lse = np.zeros((B, Hq, Sq))
     qi = np.arange(Sq)[:, None]
     kj = np.arange(Skv)[None, :]
-    visible = (kj <= qi + (Skv - Sq)) if causal else np.ones((Sq, Skv), dtype=bool)
+    if int(causal) == 1:      # bottom-right aligned
+        visible = kj <= qi + (Skv - Sq)
+    elif int(causal) == 2:    # top-left aligned
+        visible = kj <= qi
+    else:
+        visible = np.ones((Sq, Skv), dtype=bool)
     for b in range(B):
         for h in range(Hq):
             g = h // group

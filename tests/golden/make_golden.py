@@ -27,7 +27,7 @@ CASES = [
 def main():
     for (name, B, Sq, Skv, Hq, Hkv, D, causal, scale, seed, qs) in CASES:
         q, k, v = inputs.make_qkv(B, Sq, Skv, Hq, Hkv, D, seed=seed, q_sigma=qs)
-        o, lse = oracle.attn_full(q, k, v, bool(causal), scale)
+        o, lse = oracle.attn_full(q, k, v, int(causal), scale)
         rec = {"case": name, "B": B, "Sq": Sq, "Skv": Skv, "Hq": Hq, "Hkv": Hkv, "D": D,
                "causal": causal, "scale": scale, "seed": seed, "q_sigma": qs,
                "source": "oracle/oracle.c via tests/golden/make_golden.py",

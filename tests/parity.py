@@ -56,13 +56,13 @@ def compare(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
 
 def check_full(q, k, v, causal, scale, what=""):
     o_gpu, l_gpu = run_gpu(q, k, v, causal, scale)
-    o_ref, l_ref = oracle.attn_full(q, k, v, bool(causal), scale)
+    o_ref, l_ref = oracle.attn_full(q, k, v, int(causal), scale)
     return compare(o_gpu, l_gpu, o_ref, l_ref, what)
 
 
 def check_rows(q, k, v, causal, scale, rows, what=""):
     """Full-size run; the oracle computes only the listed (b, h, i) rows."""
     o_gpu, l_gpu = run_gpu(q, k, v, causal, scale)
-    o_ref, l_ref = oracle.attn_rows(q, k, v, rows, bool(causal), scale)
+    o_ref, l_ref = oracle.attn_rows(q, k, v, rows, int(causal), scale)
     b, h, i = rows[:, 0], rows[:, 1], rows[:, 2]
     return compare(o_gpu[b, i, h, :], l_gpu[b, h, i], o_ref, l_ref, what)

@@ -17,7 +17,7 @@ def test_oracle_matches_fixture(path):
     rec = json.load(open(path))
     q, k, v = inputs.make_qkv(rec["B"], rec["Sq"], rec["Skv"], rec["Hq"], rec["Hkv"], rec["D"],
                               seed=rec["seed"], q_sigma=rec["q_sigma"])
-    o, lse = oracle.attn_full(q, k, v, bool(rec["causal"]), rec["scale"])
+    o, lse = oracle.attn_full(q, k, v, int(rec["causal"]), rec["scale"])
     want_o = np.array([float.fromhex(x) for x in rec["o"]])
     want_l = np.array([float.fromhex(x) for x in rec["lse"]])
     # summation order is fixed, so only libm's exp/log may differ (<= a few ulp)

@@ -44,6 +44,10 @@ SMALL = [
     (1, 300, 77, 160, 160, 1, 1.0),     # row pairs: one tile of every unit sees no key
     (1, 300, 77, 320, 160, 1, 1.0),     # head pairs: whole units without any key
     (1, 17, 33, 320, 320, 0, 1.0),      # row pairs: tile 1 of every unit is past Sq
+    # top-left causal (causal = 2) with Sq != Skv
+    (2, 200, 333, 4, 2, 2, 1.0),
+    (1, 333, 200, 4, 4, 2, 1.0),
+    (1, 640, 1500, 8, 2, 2, 4.0),
 ]
 
 

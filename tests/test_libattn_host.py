@@ -60,7 +60,7 @@ def call(**over):
 @pytest.mark.parametrize("over", [
     dict(q=0), dict(k=0), dict(v=0), dict(o=0),
     dict(B=0), dict(Sq=0), dict(Skv=-1), dict(Hq=0), dict(Hkv=0), dict(D=0),
-    dict(Hq=6, Hkv=4), dict(causal=2), dict(causal=-1),
+    dict(Hq=6, Hkv=4), dict(causal=3), dict(causal=-1),
     dict(scale=0.0), dict(scale=-1.0), dict(scale=math.nan), dict(scale=math.inf),
     dict(q=Q + 8), dict(k=K + 2), dict(v=V + 4), dict(o=O + 1), dict(lse=L + 2),
     dict(o=Q + 64), dict(o=K), dict(lse=O + 16),
@@ -92,3 +92,30 @@ def test_library_does_not_link_the_oracle(lib):
     for name in ("oracle_attn_rows", "oracle_attn_fwd", "oracle_partial_triple"):
         assert not hasattr(lib, name)
     assert ctypes.CDLL(fa.library_path()) is not None
+
+
+def call_split(**over):
+    a = {**GOOD, "ws": 0x6000000, "ws_bytes": 1 << 20, **over}
+    return fa.attn_fwd_splitkv_ptr(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Sq"],
+                                   a["Skv"], a["Hq"], a["Hkv"], a["D"], a["causal"], a["scale"],
+                                   a["ws"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("over", [
+    dict(q=0), dict(o=0), dict(B=0), dict(Hq=6, Hkv=4), dict(causal=3), dict(scale=0.0),
+    dict(q=Q + 8), dict(o=Q), dict(ws=0x6000000 + 16),
+], ids=lambda d: ",".join(f"{k}={v}" for k, v in d.items()))
+def test_splitkv_invalid_arguments_rejected(lib, over):
+    assert call_split(**over) == fa.ATTN_ERR_INVALID_ARG
+
+
+def test_splitkv_other_head_dims_unsupported(lib):
+    assert call_split(D=64) == fa.ATTN_ERR_UNSUPPORTED
+
+
+def test_splitkv_workspace_size_argument_checks(lib):
+    assert lib.attn_fwd_splitkv_workspace_size(1, 256, 256, 2, 2, 128, 1, None) == \
+        fa.ATTN_ERR_INVALID_ARG
+    with pytest.raises(fa.AttnError) as e:
+        fa.attn_fwd_splitkv_workspace_size(1, 256, 256, 3, 2, 128, 1)
+    assert e.value.status == fa.ATTN_ERR_INVALID_ARG

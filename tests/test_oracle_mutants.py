@@ -16,8 +16,12 @@ SRC = os.path.join(os.path.dirname(HERE), "oracle", "oracle.c")
 MUTANTS = [
     ("drop_scale", "double s = p->scale * acc;", "double s = acc;"),
     ("gqa_modulo", "const long g = h / (p->Hq / p->Hkv);", "const long g = h % p->Hkv;"),
-    ("mask_off_by_one", "long end = i + (p->Skv - p->Sq) + 1;", "long end = i + (p->Skv - p->Sq);"),
-    ("top_left_mask", "long end = i + (p->Skv - p->Sq) + 1;", "long end = i + 1;"),
+    ("mask_off_by_one", "long end = (p->causal == 1) ? i + (p->Skv - p->Sq) + 1 : i + 1;",
+     "long end = (p->causal == 1) ? i + (p->Skv - p->Sq) : i;"),
+    ("bottom_right_as_top_left", "long end = (p->causal == 1) ? i + (p->Skv - p->Sq) + 1 : i + 1;",
+     "long end = i + 1;"),
+    ("top_left_as_bottom_right", "long end = (p->causal == 1) ? i + (p->Skv - p->Sq) + 1 : i + 1;",
+     "long end = i + (p->Skv - p->Sq) + 1;"),
     ("base2_lse", "= m + log(l);", "= m + log2(l);"),
     ("no_normalise", "for (long d = 0; d < D; ++d) o[d] /= l;", ";"),
     ("exp2_weights", "double w = exp(s_buf[j - j_lo] - m);", "double w = exp2(s_buf[j - j_lo] - m);"),
@@ -36,7 +40,7 @@ PIN_TESTS = [
     "test_causal_row0_is_v0", "test_one_hot_limit_pins_operand_roles", "test_matches_scipy_softmax",
     "test_brute_force_twin", "test_gqa_head_repeat_equivalence",
     "test_bottom_right_equals_tail_of_square_causal", "test_shift_invariance_large_logits",
-    "test_merge_identity_random_chunks",
+    "test_merge_identity_random_chunks", "test_top_left_rules",
 ]
 
 

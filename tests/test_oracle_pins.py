@@ -82,11 +82,12 @@ def test_hand_worked_two_keys():
     assert np.allclose(o2[0, 1, 0], [0.5, 1.5], atol=1e-15)
 
 
-@pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("Sq,Skv", [(64, 64), (16, 64), (1, 7)])
+@pytest.mark.parametrize("causal", [0, 1, 2])
+@pytest.mark.parametrize("Sq,Skv", [(64, 64), (16, 64), (1, 7), (40, 13)])
 def test_zero_query_closed_form(causal, Sq, Skv):
     """Q = 0: every visible logit is 0, so lse = ln(#visible) and o = mean of the
-    visible V rows (a cumulative mean under the bottom-right causal mask)."""
+    visible V rows (a cumulative mean under either causal mask); rows that see no
+    key get o = 0 and lse = -inf."""
     rng = np.random.default_rng(1)
     B, Hq, Hkv, D = 2, 2, 1, 128
     q = np.zeros((B, Sq, Hq, D), dtype=np.uint16)  # +0.0 in bf16
@@ -97,7 +98,10 @@ def test_zero_query_closed_form(causal, Sq, Skv):
     for b in range(B):
         for h in range(Hq):
             for i in range(Sq):
-                n = min(Skv, i + Skv - Sq + 1) if causal else Skv
+                n = {0: Skv, 1: min(Skv, i + Skv - Sq + 1), 2: min(Skv, i + 1)}[causal]
+                if n <= 0:
+                    assert np.isneginf(lse[b, h, i]) and np.all(o[b, i, h] == 0.0)
+                    continue
                 assert abs(lse[b, h, i] - math.log(n)) < 1e-13
                 want = vf[b, :n, 0, :].mean(axis=0)
                 assert np.max(np.abs(o[b, i, h] - want)) < 1e-13
@@ -170,7 +174,7 @@ def test_matches_scipy_softmax():
             assert np.max(np.abs(lse[0, h] - special.logsumexp(z, axis=1))) < 1e-13
 
 
-@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("causal", [0, 1, 2])
 @pytest.mark.parametrize("shape", [
     (1, 1, 1, 1, 1), (1, 2, 2, 2, 1), (1, 3, 3, 2, 2), (2, 17, 17, 4, 2), (1, 64, 64, 4, 1),
     (1, 256, 256, 2, 2), (1, 17, 40, 4, 4), (1, 40, 17, 2, 1),
@@ -331,3 +335,21 @@ def test_merge_rule_closed_form():
     assert abs(lse - math.log(math.exp(2.0) + math.exp(0.5))) < 1e-15
     empty = (-np.inf, 0.0, np.zeros(1))
     assert oracle.merge_triples(empty, t2)[0] == 0.5
+
+
+def test_top_left_rules():
+    """Top-left (causal=2) equals bottom-right when Sq == Skv; with Sq > Skv the
+    rows i >= Skv - 1 see every key (non-causal), with Sq < Skv row i sees keys
+    0..i only (the prefix problem)."""
+    B, H, D = 1, 2, 128
+    q, k, v = inputs.make_qkv(B, 30, 30, H, H, D, seed=31)
+    assert np.array_equal(oracle.attn_full(q, k, v, 1, 0.09)[0], oracle.attn_full(q, k, v, 2, 0.09)[0])
+    q, k, v = inputs.make_qkv(B, 40, 13, H, H, D, seed=32)
+    o_tl, l_tl = oracle.attn_full(q, k, v, 2, 0.09)
+    o_nc, l_nc = oracle.attn_full(q, k, v, 0, 0.09)
+    assert np.array_equal(o_tl[:, 12:], o_nc[:, 12:]) and np.array_equal(l_tl[:, :, 12:], l_nc[:, :, 12:])
+    q, k, v = inputs.make_qkv(B, 9, 50, H, H, D, seed=33)
+    o_tl, l_tl = oracle.attn_full(q, k, v, 2, 0.09)
+    kk, vv = np.ascontiguousarray(k[:, :9]), np.ascontiguousarray(v[:, :9])
+    o_sq, l_sq = oracle.attn_full(q, kk, vv, 1, 0.09)
+    assert np.array_equal(o_tl, o_sq) and np.array_equal(l_tl, l_sq)
