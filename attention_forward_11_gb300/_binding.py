@@ -20,8 +20,9 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_NAME = "libattn.so"
 
 # Every symbol include/attn.h declares (checked by the CPU tests).
-EXPORTED = ("attn_fwd", "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_size", "attn_status_str",
-            "attn_check_device_status", "attn_kernel_launches", "attn_debug_wait_timeout")
+EXPORTED = ("attn_fwd", "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_size",
+            "attn_fwd_splitkv_noalloc", "attn_status_str", "attn_check_device_status",
+            "attn_kernel_launches", "attn_debug_wait_timeout")
 
 _lock = threading.Lock()
 _lib = None
@@ -70,6 +71,9 @@ def load_library():
         lib.attn_fwd_splitkv.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, ctypes.c_float, P,
                                          ctypes.c_size_t, P]
         lib.attn_fwd_splitkv.restype = I
+        lib.attn_fwd_splitkv_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I,
+                                                 ctypes.c_float, P]
+        lib.attn_fwd_splitkv_noalloc.restype = I
         _lib = lib
         return lib
 
@@ -178,6 +182,16 @@ def attn_fwd_splitkv(q, k, v, o=None, lse=None, causal: int = 0, scale: float | 
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_splitkv")
     return o, lse
+
+
+def attn_fwd_splitkv_noalloc_ptr(q: int, k: int, v: int, o: int, lse: int, B: int, Sq: int,
+                                 Skv: int, Hq: int, Hkv: int, D: int, causal: int, scale: float,
+                                 stream: int) -> int:
+    """Raw-pointer call of attn_fwd_splitkv_noalloc, the split-KV entry point for
+    callers that cannot allocate device memory: its scratch is a static array
+    inside libattn.  Returns the attn_status_t value."""
+    return int(load_library().attn_fwd_splitkv_noalloc(q, k, v, o, lse, B, Sq, Skv, Hq, Hkv, D,
+                                                       causal, ctypes.c_float(scale), stream))
 
 
 def attn_check_device_status(stream=None) -> int:

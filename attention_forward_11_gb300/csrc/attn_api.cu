@@ -331,6 +331,124 @@ extern "C" attn_status_t attn_fwd_splitkv(const void* q, const void* k, const vo
     return plan->split ? launch_split(tm, p, *plan, workspace, stream) : launch_plain(tm, p, sms, stream);
 }
 
+// ---- split-KV without any allocation: scratch in a static device array
+//
+// For callers that cannot allocate device memory at the point they run
+// attention -- for example code whose device memory all belongs to another
+// allocator (a framework's caching pool, a fixed arena set up at start-up) or
+// runtimes that forbid allocation once serving has begun.  The split-KV scratch
+// then lives in this file-scope array instead of a caller workspace.  Every GPU
+// that loads the library holds the array until the process exits.
+constexpr size_t kStaticScratchBytes = size_t(40) << 20;  // 40 MiB
+static __device__ __align__(256) unsigned char g_splitkv_scratch[kStaticScratchBytes];
+
+namespace {
+
+// Device address of the static scratch on `dev` (the current device), looked up
+// once per device: in host code the array's name is only a stand-in.
+void* static_scratch_address(int dev) {
+    static std::mutex mu;
+    static void* addr[kMaxDevices] = {};
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_splitkv_scratch) != cudaSuccess || ptr == nullptr) return nullptr;
+        addr[dev] = ptr;
+    }
+    return addr[dev];
+}
+
+// The split plan of build_split_plan, computed in fixed-size storage (no heap).
+void build_split_plan_fixed(const attn::FwdParams& p, int sms, SplitPlan* plan) {
+    plan->split = false;
+    if (p.n_units < 1 || p.n_units > attn::kMaxPieces) return;
+    int W[attn::kMaxPieces];
+    long long bnd[attn::kMaxSplitCtas + 1];
+    unsigned short piece_cta[attn::kMaxPieces];
+    long long T = 0;
+    for (int u = 0; u < p.n_units; ++u) {
+        W[u] = attn::decode_unit(p, u).nmax();
+        if (W[u] > 0xFFFF) return;
+        T += W[u];
+    }
+    const int G = static_cast<int>(std::min<long long>(std::min(sms, attn::kMaxSplitCtas), T));
+    if (G < 1) return;
+    for (int c = 0; c <= G; ++c) bnd[c] = (long long)c * T / G;
+    attn::SplitSched& sc = plan->sched;
+    attn::CombineTable& cb = plan->comb;
+    int n_pieces = 0, n_slots = 0, n_comb = 0, c = 0;
+    long long off = 0;
+    auto add = [&](int u, int kb, int ke, int slot, int cta) -> bool {
+        if (n_pieces >= attn::kMaxPieces) return false;
+        sc.piece[n_pieces] = attn::Piece{u, static_cast<unsigned int>(kb) | (static_cast<unsigned int>(ke) << 16),
+                                         slot};
+        piece_cta[n_pieces++] = static_cast<unsigned short>(cta);
+        return true;
+    };
+    for (int u = 0; u < p.n_units; ++u) {
+        const long long a = off, e = off + W[u];
+        while (c < G - 1 && a >= bnd[c + 1]) ++c;
+        if (W[u] == 0) {
+            if (!add(u, 0, 0, -1, c)) return;
+            continue;
+        }
+        int c1 = c;
+        while (c1 < G - 1 && e > bnd[c1 + 1]) ++c1;
+        if (c1 == c) {
+            if (!add(u, 0, W[u], -1, c)) return;
+        } else {
+            if (n_comb >= attn::kMaxCombine) return;
+            cb.e[n_comb++] = attn::CombineEntry{u, n_slots, c1 - c + 1};
+            for (int cc = c; cc <= c1; ++cc) {
+                const long long kb = std::max(a, bnd[cc]) - a, ke = std::min(e, bnd[cc + 1]) - a;
+                if (!add(u, static_cast<int>(kb), static_cast<int>(ke), n_slots++, cc)) return;
+            }
+        }
+        off = e;
+    }
+    if (n_comb == 0) return;
+    int i = 0;
+    for (int cc = 0; cc <= G; ++cc) {
+        while (i < n_pieces && piece_cta[i] < cc) ++i;
+        sc.cta_begin[cc] = static_cast<unsigned short>(i);
+    }
+    sc.n_pieces = n_pieces;
+    cb.n = n_comb;
+    plan->grid = G;
+    plan->n_slots = n_slots;
+    plan->split = true;
+}
+
+}  // namespace
+
+extern "C" attn_status_t attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
+                                                  float* lse, int B, int Sq, int Skv, int Hq, int Hkv, int D,
+                                                  int causal, float scale, cudaStream_t stream) {
+    if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+    attn_status_t st = check_sizes(B, Sq, Skv, Hq, Hkv, D, causal);
+    if (st == ATTN_ERR_INVALID_ARG) return st;
+    const attn_status_t sp = check_pointers(q, k, v, o, lse, B, Sq, Skv, Hq, Hkv, D > 0 ? D : 1);
+    if (sp != ATTN_OK) return sp;
+    attn::FwdParams p{};
+    const attn_status_t sm = make_params(B, Sq, Skv, Hq, Hkv, causal, scale, o, lse, &p);
+    if (sm != ATTN_OK) return sm;
+    if (st != ATTN_OK) return st;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || !device_setup(dev, &sms)) return ATTN_ERR_CUDA;
+    void* scratch = static_scratch_address(dev);  // first call on a device: one-time look-up
+    if (scratch == nullptr) return ATTN_ERR_CUDA;
+    // the plan lives in static storage: one call at a time builds and launches it
+    static std::mutex plan_mu;
+    static SplitPlan plan;
+    std::lock_guard<std::mutex> lock(plan_mu);
+    build_split_plan_fixed(p, sms, &plan);
+    if (plan.split && workspace_bytes_for(plan.n_slots) > kStaticScratchBytes) return ATTN_ERR_UNSUPPORTED;
+    CUtensorMap tm[4];
+    if (!encode_maps(q, k, v, o, B, Sq, Skv, Hq, Hkv, D, tm)) return ATTN_ERR_CUDA;
+    return plan.split ? launch_split(tm, p, plan, scratch, stream) : launch_plain(tm, p, sms, stream);
+}
+
 extern "C" const char* attn_status_str(attn_status_t status) {
     switch (status) {
         case ATTN_OK: return "ATTN_OK";

@@ -91,6 +91,31 @@ attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void
                                float scale, void* workspace, size_t workspace_bytes,
                                cudaStream_t stream);
 
+/*
+ * attn_fwd_splitkv_noalloc -- attn_fwd_splitkv for callers that cannot
+ * allocate device memory where they call attention: code whose device memory
+ * all belongs to another allocator (a framework's caching pool, a fixed arena
+ * reserved at start-up) or that runs where allocation is not allowed once
+ * serving has begun.  The pages have no counterpart of this entry point.
+ *
+ * Same arguments, semantics and errors as attn_fwd_splitkv, without the
+ * workspace: the split-KV scratch is a static 40 MiB device array inside
+ * libattn, which every GPU that loads the library holds until the process
+ * exits.  The call allocates nothing, on the device or on the host.
+ *   - The first call on a device looks up that array's device address (once per
+ *     device, with the device current); make that first call before any stream
+ *     capture begins.
+ *   - Problems whose scratch would exceed 40 MiB return ATTN_ERR_UNSUPPORTED
+ *     (on a 152-SM GPU the split plan never needs more than about 38.4 MiB).
+ *   - Every call shares the one array, which keeps the last call's contents;
+ *     nothing in it needs to start at zero (each call writes every partial slot
+ *     before it reads it).  Calls that overlap in time on the GPU (different
+ *     streams, or devices sharing the process's array) race on it: serialise them.
+ */
+attn_status_t attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
+                                       float* lse, int B, int Sq, int Skv, int Hq, int Hkv, int D,
+                                       int causal, float scale, cudaStream_t stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char* attn_status_str(attn_status_t status);
 
