@@ -15,12 +15,14 @@ ATTN_ERR_INVALID_ARG = 1
 ATTN_ERR_UNSUPPORTED = 2
 ATTN_ERR_CUDA = 3
 ATTN_ERR_TIMEOUT = 4
+ATTN_DTYPE_BF16 = 0
+ATTN_DTYPE_F16 = 1
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_NAME = "libattn.so"
 
 # Every symbol include/attn.h declares (checked by the CPU tests).
-EXPORTED = ("attn_fwd", "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_size",
+EXPORTED = ("attn_fwd", "attn_fwd_ex", "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_size",
             "attn_fwd_splitkv_noalloc", "attn_status_str", "attn_check_device_status",
             "attn_kernel_launches", "attn_debug_wait_timeout")
 
@@ -57,6 +59,8 @@ def load_library():
         I = ctypes.c_int
         lib.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, ctypes.c_float, P]
         lib.attn_fwd.restype = I
+        lib.attn_fwd_ex.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, ctypes.c_float, I, P]
+        lib.attn_fwd_ex.restype = I
         lib.attn_status_str.argtypes = [I]
         lib.attn_status_str.restype = ctypes.c_char_p
         lib.attn_check_device_status.argtypes = [P]
@@ -103,11 +107,19 @@ def attn_fwd_ptr(q: int, k: int, v: int, o: int, lse: int, B: int, Sq: int, Skv:
                                        ctypes.c_float(scale), stream))
 
 
+def attn_fwd_ex_ptr(q: int, k: int, v: int, o: int, lse: int, B: int, Sq: int, Skv: int, Hq: int,
+                    Hkv: int, D: int, causal: int, scale: float, dtype: int, stream: int) -> int:
+    """Raw-pointer call of attn_fwd_ex (dtype: ATTN_DTYPE_BF16 or ATTN_DTYPE_F16)."""
+    return int(load_library().attn_fwd_ex(q, k, v, o, lse, B, Sq, Skv, Hq, Hkv, D, causal,
+                                          ctypes.c_float(scale), dtype, stream))
+
+
 def attn_fwd(q, k, v, o=None, lse=None, causal: int = 0, scale: float | None = None,
              stream=None, want_lse: bool = True):
     """O = softmax(scale * Q K^T [+ causal mask]) V and its fp32 log-sum-exp.
 
-    q: bf16 CUDA tensor [B, Sq, Hq, D]; k, v: [B, Skv, Hkv, D]; all contiguous.
+    q: bf16 or float16 CUDA tensor [B, Sq, Hq, D]; k, v: [B, Skv, Hkv, D], same
+    dtype; all contiguous.
     o (optional): bf16 [B, Sq, Hq, D]; lse (optional): fp32 [B, Hq, Sq].
     causal: 0 none, 1 bottom-right aligned, 2 top-left aligned.  Returns (o, lse or None).
     Runs asynchronously on ``stream`` (default: torch's current stream).
@@ -117,20 +129,26 @@ def attn_fwd(q, k, v, o=None, lse=None, causal: int = 0, scale: float | None = N
         raise AttnError(ATTN_ERR_INVALID_ARG, "q, k, v must be 4-d [B, S, H, D]")
     B, Sq, Hq, D = q.shape
     Skv, Hkv = k.shape[1], k.shape[2]
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise AttnError(ATTN_ERR_INVALID_ARG, "q must be bf16 or float16")
     for name, t in (("q", q), ("k", k), ("v", v)):
-        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
-            raise AttnError(ATTN_ERR_INVALID_ARG, f"{name} must be a contiguous bf16 CUDA tensor")
+        if t.dtype != q.dtype or not t.is_cuda or not t.is_contiguous():
+            raise AttnError(ATTN_ERR_INVALID_ARG,
+                            f"{name} must be a contiguous CUDA tensor of q's dtype")
     if tuple(v.shape) != tuple(k.shape) or k.shape[0] != B or k.shape[3] != D:
         raise AttnError(ATTN_ERR_INVALID_ARG, "k/v shapes do not match q")
     if o is None:
         o = torch.empty_like(q)
+    if o.dtype != q.dtype:
+        raise AttnError(ATTN_ERR_INVALID_ARG, "o must have q's dtype")
     if lse is None and want_lse:
         lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
     if scale is None:
         scale = 1.0 / (D ** 0.5)
-    st = attn_fwd_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                      lse.data_ptr() if lse is not None else 0, B, Sq, Skv, Hq, Hkv, D,
-                      int(causal), float(scale), _stream_handle(stream))
+    dtype = ATTN_DTYPE_F16 if q.dtype == torch.float16 else ATTN_DTYPE_BF16
+    st = attn_fwd_ex_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                         lse.data_ptr() if lse is not None else 0, B, Sq, Skv, Hq, Hkv, D,
+                         int(causal), float(scale), dtype, _stream_handle(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd")
     return o, lse

@@ -47,7 +47,7 @@ EncodeTiledFn encoder() {
 // 4-d view [B, S, H, D] of a bf16 tensor (D innermost), 128-row x 64-column
 // boxes with 128-byte swizzle: the layout the tcgen05 K-major / MN-major
 // shared-memory descriptors expect.
-bool encode_bshd(CUtensorMap* map, const void* ptr, int B, int S, int H, int D) {
+bool encode_bshd(CUtensorMap* map, const void* ptr, int B, int S, int H, int D, bool f16 = false) {
     EncodeTiledFn fn = encoder();
     if (!fn) return false;
     const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
@@ -55,7 +55,8 @@ bool encode_bshd(CUtensorMap* map, const void* ptr, int B, int S, int H, int D) 
                                    (cuuint64_t)S * H * D * 2};
     const cuuint32_t box[4] = {64, 1, (cuuint32_t)attn::kBM, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box,
+    return fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+              const_cast<void*>(ptr), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -68,9 +69,11 @@ bool device_setup(int dev, int* sm_count) {
     std::lock_guard<std::mutex> lock(mu);
     if (sms[dev] == 0) {
         int n = 0;
-        if (cudaFuncSetAttribute(attn::fmha_fwd_kernel<attn::PlainSched>,
+        if (cudaFuncSetAttribute(attn::fmha_fwd_kernel<attn::PlainSched, false>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, attn::kSmemBytes) != cudaSuccess ||
-            cudaFuncSetAttribute(attn::fmha_fwd_kernel<attn::SplitSched>,
+            cudaFuncSetAttribute(attn::fmha_fwd_kernel<attn::PlainSched, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, attn::kSmemBytes) != cudaSuccess ||
+            cudaFuncSetAttribute(attn::fmha_fwd_kernel<attn::SplitSched, false>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, attn::kSmemBytes) != cudaSuccess ||
             cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
             return false;
@@ -146,9 +149,9 @@ attn_status_t make_params(int B, int Sq, int Skv, int Hq, int Hkv, int causal, f
 }
 
 bool encode_maps(const void* q, const void* k, const void* v, const void* o, int B, int Sq, int Skv, int Hq,
-                 int Hkv, int D, CUtensorMap* tm) {
-    return encode_bshd(&tm[0], q, B, Sq, Hq, D) && encode_bshd(&tm[1], k, B, Skv, Hkv, D) &&
-           encode_bshd(&tm[2], v, B, Skv, Hkv, D) && encode_bshd(&tm[3], o, B, Sq, Hq, D);
+                 int Hkv, int D, CUtensorMap* tm, bool f16 = false) {
+    return encode_bshd(&tm[0], q, B, Sq, Hq, D, f16) && encode_bshd(&tm[1], k, B, Skv, Hkv, D, f16) &&
+           encode_bshd(&tm[2], v, B, Skv, Hkv, D, f16) && encode_bshd(&tm[3], o, B, Sq, Hq, D, f16);
 }
 
 // ---- split-KV plan: equal contiguous shares of the (unit, KV tile) iterations
@@ -230,10 +233,11 @@ void build_split_plan(const attn::FwdParams& p, int sms, SplitPlan* plan) {
     plan->split = true;
 }
 
+template <bool kF16 = false>
 attn_status_t launch_plain(const CUtensorMap* tm, const attn::FwdParams& p, int sms, cudaStream_t stream) {
     // persistent grid: at most one CTA per SM (the CTA holds all 512 TMEM columns)
     const int grid = p.n_units < sms ? p.n_units : sms;
-    attn::fmha_fwd_kernel<attn::PlainSched><<<static_cast<unsigned int>(grid), attn::kThreads, attn::kSmemBytes,
+    attn::fmha_fwd_kernel<attn::PlainSched, kF16><<<static_cast<unsigned int>(grid), attn::kThreads, attn::kSmemBytes,
                                               stream>>>(tm[0], tm[1], tm[2], tm[3], p, attn::PlainSched{0});
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -246,7 +250,7 @@ attn_status_t launch_split(const CUtensorMap* tm, const attn::FwdParams& p, Spli
     const size_t o_pad = (o_bytes + kWorkspaceAlign - 1) / kWorkspaceAlign * kWorkspaceAlign;
     plan.sched.ws_o = static_cast<float*>(workspace);
     plan.sched.ws_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) + o_pad);
-    attn::fmha_fwd_kernel<attn::SplitSched><<<static_cast<unsigned int>(plan.grid), attn::kThreads,
+    attn::fmha_fwd_kernel<attn::SplitSched, false><<<static_cast<unsigned int>(plan.grid), attn::kThreads,
                                               attn::kSmemBytes, stream>>>(tm[0], tm[1], tm[2], tm[3], p, plan.sched);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -255,7 +259,7 @@ attn_status_t launch_split(const CUtensorMap* tm, const attn::FwdParams& p, Spli
     plan.comb.o = p.o;
     const long long warps = (long long)plan.comb.n * attn::kTiles * attn::kBM;
     const unsigned int blocks = static_cast<unsigned int>((warps + attn::kCombineWarps - 1) / attn::kCombineWarps);
-    attn::splitkv_combine_kernel<<<blocks, 32 * attn::kCombineWarps, 0, stream>>>(p, plan.comb);
+    attn::splitkv_combine_kernel<false><<<blocks, 32 * attn::kCombineWarps, 0, stream>>>(p, plan.comb);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return ATTN_OK;
@@ -263,9 +267,10 @@ attn_status_t launch_split(const CUtensorMap* tm, const attn::FwdParams& p, Spli
 
 }  // namespace
 
-extern "C" attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
-                                  int B, int Sq, int Skv, int Hq, int Hkv, int D, int causal,
-                                  float scale, cudaStream_t stream) {
+namespace {
+
+attn_status_t fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Sq, int Skv,
+                       int Hq, int Hkv, int D, int causal, float scale, bool f16, cudaStream_t stream) {
     // ---- validation: nothing is launched on any error
     if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
     attn_status_t st = check_sizes(B, Sq, Skv, Hq, Hkv, D, causal);
@@ -277,10 +282,25 @@ extern "C" attn_status_t attn_fwd(const void* q, const void* k, const void* v, v
     if (sm != ATTN_OK) return sm;
     if (st != ATTN_OK) return st;  // valid request, unsupported head size
     CUtensorMap tm[4];
-    if (!encode_maps(q, k, v, o, B, Sq, Skv, Hq, Hkv, D, tm)) return ATTN_ERR_CUDA;
+    if (!encode_maps(q, k, v, o, B, Sq, Skv, Hq, Hkv, D, tm, f16)) return ATTN_ERR_CUDA;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || !device_setup(dev, &sms)) return ATTN_ERR_CUDA;
-    return launch_plain(tm, p, sms, stream);
+    return f16 ? launch_plain<true>(tm, p, sms, stream) : launch_plain<false>(tm, p, sms, stream);
+}
+
+}  // namespace
+
+extern "C" attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                                  int B, int Sq, int Skv, int Hq, int Hkv, int D, int causal,
+                                  float scale, cudaStream_t stream) {
+    return fwd_impl(q, k, v, o, lse, B, Sq, Skv, Hq, Hkv, D, causal, scale, false, stream);
+}
+
+extern "C" attn_status_t attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                                     int Sq, int Skv, int Hq, int Hkv, int D, int causal, float scale, int dtype,
+                                     cudaStream_t stream) {
+    if (dtype != ATTN_DTYPE_BF16 && dtype != ATTN_DTYPE_F16) return ATTN_ERR_INVALID_ARG;
+    return fwd_impl(q, k, v, o, lse, B, Sq, Skv, Hq, Hkv, D, causal, scale, dtype == ATTN_DTYPE_F16, stream);
 }
 
 extern "C" attn_status_t attn_fwd_splitkv_workspace_size(int B, int Sq, int Skv, int Hq, int Hkv, int D,

@@ -280,7 +280,8 @@ __device__ __forceinline__ bool get_work(const FwdParams& p, const SplitSched& s
     return true;
 }
 
-template <class Sched>
+// kF16: Q, K, V, O are IEEE binary16 instead of bf16 (P follows the operands).
+template <class Sched, bool kF16>
 __global__ void __launch_bounds__(kThreads, 1)
     fmha_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -407,8 +408,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // =========================== MMA issuer =============================
         // The whole warp runs the control flow (so descriptors and stage indices stay
         // warp-uniform); one elected lane issues each group of MMAs and its commits.
-        constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, false);
-        constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, kHeadDim, true);
+        constexpr uint32_t idesc_qk = idesc_f16kind_f32(kBM, kBN, false, kF16);
+        constexpr uint32_t idesc_pv = idesc_f16kind_f32(kBM, kHeadDim, true, kF16);
         // descriptor of k-step kk = base descriptor + constant start-address offset (>> 4)
         const uint64_t q_desc0 = sdesc_sw128(sbase + kSmemQ, 16, 1024);
         const uint64_t k_desc0 = sdesc_sw128(sbase + kSmemK, 16, 1024);
@@ -670,8 +671,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 fadd2_acc(rs0, rs1, a0, a1);
                                 fadd2_acc(rs0, rs1, b0, b1);
                             }
-                            pk[q] = pack_bf16x2(a0, a1);
-                            pk[q + 1] = pack_bf16x2(b0, b1);
+                            pk[q] = pack_x2<kF16>(a0, a1);
+                            pk[q + 1] = pack_x2<kF16>(b0, b1);
                         }
                         tmem_st16(tS + 16 * c, pk);
                     }
@@ -777,8 +778,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             fmul2_b(f[e], f[e + 1], __uint_as_float(o[8 * q + e]), __uint_as_float(o[8 * q + e + 1]),
                                     inv_l);
                         *reinterpret_cast<uint4*>(stage + r * 128 + ((q ^ (r & 7)) * 16)) =
-                            make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
-                                       pack_bf16x2(f[6], f[7]));
+                            make_uint4(pack_x2<kF16>(f[0], f[1]), pack_x2<kF16>(f[2], f[3]),
+                                       pack_x2<kF16>(f[4], f[5]), pack_x2<kF16>(f[6], f[7]));
                     }
                     fence_proxy_async_smem();
                     named_bar_sync(1, 128);
@@ -821,11 +822,12 @@ constexpr int kCombineWarps = 8;
 struct CombineTable {
     const float* ws_o;
     const float2* ws_ml;
-    uint16_t* o;          // [B, Sq, Hq, D] bf16
+    uint16_t* o;          // [B, Sq, Hq, D] bf16 or f16
     int n;
     CombineEntry e[kMaxCombine];
 };
 
+template <bool kF16>
 __global__ void __launch_bounds__(32 * kCombineWarps)
     splitkv_combine_kernel(const FwdParams p, const __grid_constant__ CombineTable ct) {
     const int gw = static_cast<int>(blockIdx.x) * kCombineWarps + static_cast<int>(threadIdx.x) / 32;
@@ -859,8 +861,8 @@ __global__ void __launch_bounds__(32 * kCombineWarps)
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
     uint2 out;
-    out.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-    out.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+    out.x = pack_x2<kF16>(acc.x * inv, acc.y * inv);
+    out.y = pack_x2<kF16>(acc.z * inv, acc.w * inv);
     reinterpret_cast<uint2*>(ct.o + ((static_cast<size_t>(w.b) * p.Sq + row) * p.Hq + w.hq(t)) * kHeadDim)[lane] = out;
     if (lane == 0 && p.lse != nullptr)
         p.lse[(static_cast<size_t>(w.b) * p.Hq + w.hq(t)) * p.Sq + row] =

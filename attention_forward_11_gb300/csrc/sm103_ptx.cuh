@@ -248,13 +248,17 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
     return d;
 }
 
-// Instruction descriptor for kind::f16 with bf16 A/B and an fp32 accumulator:
-//   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format (1 = bf16),
-//   bit 15 A major (0 = K), bit 16 B major (0 = K, 1 = MN), bits 17-22 N >> 3,
-//   bits 24-28 M >> 4.
+// Instruction descriptor for kind::f16 with 16-bit A/B and an fp32 accumulator:
+//   bits 4-5 D format (1 = f32), 7-9 A format and 10-12 B format (0 = f16,
+//   1 = bf16; A and B always the same type here), bit 15 A major (0 = K),
+//   bit 16 B major (0 = K, 1 = MN), bits 17-22 N >> 3, bits 24-28 M >> 4.
+__host__ __device__ constexpr uint32_t idesc_f16kind_f32(uint32_t M, uint32_t N, bool b_mn_major,
+                                                         bool f16) {
+    return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) |
+           ((b_mn_major ? 1u : 0u) << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bool b_mn_major) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
-           ((N >> 3) << 17) | ((M >> 4) << 24);
+    return idesc_f16kind_f32(M, N, b_mn_major, false);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]
@@ -339,6 +343,20 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+// two fp32 -> packed IEEE binary16 x2 (round to nearest even); `lo` in bits 0-15
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// packed pair in the element type of the operands: f16 when kF16, else bf16
+template <bool kF16>
+__device__ __forceinline__ uint32_t pack_x2(float lo, float hi) {
+    if constexpr (kF16) return pack_f16x2(lo, hi);
+    else return pack_bf16x2(lo, hi);
 }
 
 }  // namespace attn

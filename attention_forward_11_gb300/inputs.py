@@ -61,21 +61,24 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     return r.astype(np.uint16)
 
 
-def normal_bf16(shape, sigma: float, seed: int, stream: int) -> np.ndarray:
-    """bf16 bits of N(0, sigma^2) draws from PCG64 seeded with (seed, stream)."""
+def normal_bf16(shape, sigma: float, seed: int, stream: int, dtype: str = "bf16") -> np.ndarray:
+    """16-bit patterns of N(0, sigma^2) draws from PCG64 seeded with (seed, stream):
+    bf16 (default) or IEEE binary16 ("f16", numpy's round-to-nearest-even)."""
     rng = np.random.Generator(np.random.PCG64([seed, stream]))
     x = rng.standard_normal(size=shape, dtype=np.float32)
     if sigma != 1.0:
         x *= np.float32(sigma)
+    if dtype == "f16":
+        return x.astype(np.float16).view(np.uint16)
     return f32_to_bf16_bits(x)
 
 
 def make_qkv(B, Sq, Skv, Hq, Hkv, D, seed: int = 0, q_sigma: float = 1.0,
-             kv_sigma: float = 1.0):
-    """Q [B,Sq,Hq,D], K and V [B,Skv,Hkv,D] as uint16 bf16 bits (streams 0, 1, 2)."""
-    q = normal_bf16((B, Sq, Hq, D), q_sigma, seed, 0)
-    k = normal_bf16((B, Skv, Hkv, D), kv_sigma, seed, 1)
-    v = normal_bf16((B, Skv, Hkv, D), kv_sigma, seed, 2)
+             kv_sigma: float = 1.0, dtype: str = "bf16"):
+    """Q [B,Sq,Hq,D], K and V [B,Skv,Hkv,D] as uint16 bit patterns (streams 0, 1, 2)."""
+    q = normal_bf16((B, Sq, Hq, D), q_sigma, seed, 0, dtype)
+    k = normal_bf16((B, Skv, Hkv, D), kv_sigma, seed, 1, dtype)
+    v = normal_bf16((B, Skv, Hkv, D), kv_sigma, seed, 2, dtype)
     return q, k, v
 
 

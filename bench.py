@@ -269,10 +269,12 @@ def run_ours(args, w):
         dist.barrier()
     fa.load_library()
 
-    q_h, k_h, v_h = inputs.make_workload(w, seed=rank)
+    q_h, k_h, v_h = inputs.make_qkv(w.B, w.Sq, w.Skv, w.Hq, w.Hkv, w.D, seed=rank,
+                                    q_sigma=w.q_sigma, kv_sigma=w.kv_sigma, dtype=args.dtype)
+    tdtype = torch.float16 if args.dtype == "f16" else torch.bfloat16
 
     def pinned(bits):
-        t = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+        t = torch.from_numpy(bits.view(np.int16)).view(tdtype)
         return t.pin_memory()
 
     qp, kp, vp = pinned(q_h), pinned(k_h), pinned(v_h)
@@ -281,7 +283,7 @@ def run_ours(args, w):
     v = vp.to(dev)
     o = torch.empty_like(q)
     lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
-    o_h = torch.empty(o.shape, dtype=torch.bfloat16).pin_memory()
+    o_h = torch.empty(o.shape, dtype=tdtype).pin_memory()
     lse_h = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -296,6 +298,10 @@ def run_ours(args, w):
             st = fa.attn_fwd_splitkv_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                          lse.data_ptr(), w.B, w.Sq, w.Skv, w.Hq, w.Hkv, w.D,
                                          w.causal, w.scale, ws.data_ptr(), ws_bytes, sh)
+        elif args.dtype == "f16":
+            st = fa.attn_fwd_ex_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                    lse.data_ptr(), w.B, w.Sq, w.Skv, w.Hq, w.Hkv, w.D, w.causal,
+                                    w.scale, fa.ATTN_DTYPE_F16, sh)
         else:
             st = fa.attn_fwd_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                  lse.data_ptr(), w.B, w.Sq, w.Skv, w.Hq, w.Hkv, w.D, w.causal,
@@ -371,7 +377,7 @@ def run_ours(args, w):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * mean_launch_s, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": args.dtype, "data": "synthetic",
         "config": {**w.as_dict(), "parallelism": "replicas" if world > 1 else "single",
                    "entry_point": "attn_fwd_splitkv" if args.path == "splitkv" else "attn_fwd",
                    "workspace_bytes": ws_bytes,
@@ -410,10 +416,14 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--dtype", choices=["bf16", "f16"], default="bf16",
+                    help="element type of Q, K, V, O (f16 goes through attn_fwd_ex)")
     ap.add_argument("--path", choices=["fwd", "splitkv"], default="fwd",
                     help="entry point timed: attn_fwd, or attn_fwd_splitkv with its workspace")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
+    if args.dtype == "f16" and args.path == "splitkv":
+        ap.error("the split-KV entry points take bf16")
     w = inputs.WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, w)

@@ -65,11 +65,29 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
                        int Sq, int Skv, int Hq, int Hkv, int D, int causal, float scale,
                        cudaStream_t stream);
 
+/* Element type of q, k, v and o for attn_fwd_ex. */
+typedef enum {
+    ATTN_DTYPE_BF16 = 0, /* bfloat16 (what attn_fwd takes) */
+    ATTN_DTYPE_F16 = 1   /* IEEE binary16 */
+} attn_dtype_t;
+
+/*
+ * attn_fwd_ex -- attn_fwd with a choice of 16-bit element type for q, k, v and
+ * o (the Pallas page's forward accepts float16 and bfloat16 alike).  `dtype`
+ * is an attn_dtype_t; anything else returns ATTN_ERR_INVALID_ARG.  P is rounded
+ * to the same type before the P.V product; accumulation, softmax and LSE stay
+ * fp32; O is rounded to nearest-even in that type.  Everything else, including
+ * errors, as attn_fwd.
+ */
+attn_status_t attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                          int B, int Sq, int Skv, int Hq, int Hkv, int D, int causal, float scale,
+                          int dtype, cudaStream_t stream);
+
 /*
  * Split-KV forward for problems with too few query tiles to fill the GPU
  * (short query blocks against long key ranges, e.g. chunked prefill).  The
- * same operation and arguments as attn_fwd, plus a device workspace the caller
- * allocates.  This is the single-GPU form of the kernbench page's group
+ * same operation and arguments as attn_fwd (bf16), plus a device workspace the
+ * caller allocates.  This is the single-GPU form of the kernbench page's group
  * sequence parallelism (`_gqa_attention_prefill_short.py`): the iterations over
  * (query tile pair, KV tile) are cut into equal contiguous shares, one per SM; a
  * tile pair whose KV range straddles shares is computed in pieces whose partial

@@ -53,13 +53,13 @@ def configure(lib):
     P = ctypes.c_void_p
     L = ctypes.c_long
     lib.oracle_attn_rows.argtypes = [P, P, P, L, L, L, L, L, L, ctypes.c_int,
-                                     ctypes.c_double, L, P, P, P]
+                                     ctypes.c_double, ctypes.c_int, L, P, P, P]
     lib.oracle_attn_rows.restype = ctypes.c_int
     lib.oracle_attn_fwd.argtypes = [P, P, P, L, L, L, L, L, L, ctypes.c_int,
-                                    ctypes.c_double, P, P]
+                                    ctypes.c_double, ctypes.c_int, P, P]
     lib.oracle_attn_fwd.restype = ctypes.c_int
     lib.oracle_partial_triple.argtypes = [P, P, P, L, L, L, L, L, L, ctypes.c_int,
-                                          ctypes.c_double, L, L, L, L, L, P, P, P]
+                                          ctypes.c_double, ctypes.c_int, L, L, L, L, L, P, P, P]
     lib.oracle_partial_triple.restype = ctypes.c_int
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = ctypes.c_int
@@ -96,42 +96,44 @@ def num_threads() -> int:
     return int(_load().oracle_num_threads())
 
 
-def attn_rows(q, k, v, rows, causal: int, scale: float):
+def attn_rows(q, k, v, rows, causal: int, scale: float, f16: bool = False):
     """fp64 o (len(rows) x D) and lse (len(rows)) for the listed (b, h, i) rows.
-    causal: 0 none, 1 bottom-right (j <= i + Skv - Sq), 2 top-left (j <= i)."""
+    causal: 0 none, 1 bottom-right (j <= i + Skv - Sq), 2 top-left (j <= i).
+    f16: the uint16 inputs are IEEE binary16 bit patterns instead of bf16."""
     B, Sq, Skv, Hq, Hkv, D = _check_inputs(q, k, v)
     rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
     o = np.zeros((rows.shape[0], D), dtype=np.float64)
     lse = np.zeros(rows.shape[0], dtype=np.float64)
     rc = _load().oracle_attn_rows(_ptr(q), _ptr(k), _ptr(v), B, Sq, Skv, Hq, Hkv, D,
-                                  int(causal), float(scale), rows.shape[0],
+                                  int(causal), float(scale), int(bool(f16)), rows.shape[0],
                                   _ptr(rows), _ptr(o), _ptr(lse))
     if rc != 0:
         raise ValueError("oracle_attn_rows rejected its arguments")
     return o, lse
 
 
-def attn_full(q, k, v, causal: int, scale: float):
-    """fp64 o [B,Sq,Hq,D] and lse [B,Hq,Sq] for every row."""
+def attn_full(q, k, v, causal: int, scale: float, f16: bool = False):
+    """fp64 o [B,Sq,Hq,D] and lse [B,Hq,Sq] for every row (f16: binary16 inputs)."""
     B, Sq, Skv, Hq, Hkv, D = _check_inputs(q, k, v)
     o = np.zeros((B, Sq, Hq, D), dtype=np.float64)
     lse = np.zeros((B, Hq, Sq), dtype=np.float64)
     rc = _load().oracle_attn_fwd(_ptr(q), _ptr(k), _ptr(v), B, Sq, Skv, Hq, Hkv, D,
-                                 int(causal), float(scale), _ptr(o), _ptr(lse))
+                                 int(causal), float(scale), int(bool(f16)), _ptr(o), _ptr(lse))
     if rc != 0:
         raise ValueError("oracle_attn_fwd rejected its arguments")
     return o, lse
 
 
-def partial_triple(q, k, v, causal: bool, scale: float, b: int, h: int, i: int,
-                   j_lo: int, j_hi: int):
+def partial_triple(q, k, v, causal: int, scale: float, b: int, h: int, i: int,
+                   j_lo: int, j_hi: int, f16: bool = False):
     """Un-normalised (m, l, o) of row (b, h, i) over keys [j_lo, j_hi)."""
     B, Sq, Skv, Hq, Hkv, D = _check_inputs(q, k, v)
     m = np.zeros(1, dtype=np.float64)
     l = np.zeros(1, dtype=np.float64)
     o = np.zeros(D, dtype=np.float64)
     rc = _load().oracle_partial_triple(_ptr(q), _ptr(k), _ptr(v), B, Sq, Skv, Hq, Hkv, D,
-                                       int(causal), float(scale), b, h, i, j_lo, j_hi,
+                                       int(causal), float(scale), int(bool(f16)), b, h, i,
+                                       j_lo, j_hi,
                                        _ptr(m), _ptr(l), _ptr(o))
     if rc != 0:
         raise ValueError("oracle_partial_triple rejected its arguments")
@@ -186,6 +188,39 @@ def round_bf16(x) -> np.ndarray:
     r[np.abs(r) > max_bf16] = np.copysign(np.inf, r[np.abs(r) > max_bf16])
     out[finite] = r
     return out
+
+
+def round_f16(x) -> np.ndarray:
+    """Exact round-to-nearest-even of fp64 values to IEEE binary16 (returned as fp64).
+
+    binary16 keeps 11 significant bits; normal numbers start at 2^-14, below
+    that the grid is fixed at 2^-24; past 65504 (plus half a step) values go to
+    +-inf.  Same splitting as round_bf16: x = f * 2^e, 0.5 <= |f| < 1, f * 2^11
+    rounded half-to-even.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    out = np.array(x, dtype=np.float64, copy=True)
+    finite = np.isfinite(x) & (x != 0.0)
+    xf = x[finite]
+    f, e = np.frexp(xf)
+    normal = e >= -13  # |x| >= 2^-14  <=>  e - 1 >= -14
+    r = np.empty_like(xf)
+    r[normal] = np.ldexp(np.rint(np.ldexp(f[normal], 11)), e[normal] - 11)
+    r[~normal] = np.ldexp(np.rint(np.ldexp(xf[~normal], 24)), -24)
+    r[np.abs(r) > 65504.0] = np.copysign(np.inf, r[np.abs(r) > 65504.0])
+    out[finite] = r
+    return out
+
+
+def f16_bits_to_f64(bits) -> np.ndarray:
+    """Widen IEEE binary16 bit patterns (uint16) to fp64 exactly."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.int64)
+    sign = np.where(b >> 15, -1.0, 1.0)
+    e = (b >> 10) & 0x1F
+    frac = (b & 0x3FF).astype(np.float64)
+    mag = np.where(e == 0, np.ldexp(frac, -24), np.ldexp(frac + 1024.0, e - 25))
+    mag = np.where(e == 31, np.where(frac > 0, np.nan, np.inf), mag)
+    return sign * mag
 
 
 def bf16_bits_to_f64(bits) -> np.ndarray:

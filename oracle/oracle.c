@@ -25,8 +25,9 @@
  * A row with no visible key gets o = 0 and lse = -inf (the pages leave this
  * case open; this is the reading the tests and the GPU path share).
  *
- * Inputs are raw bf16 bit patterns ([B,Sq,Hq,D] for q, [B,Skv,Hkv,D] for k and
- * v, D contiguous), widened exactly to fp64.  Nothing is blocked, fused or
+ * Inputs are raw 16-bit patterns ([B,Sq,Hq,D] for q, [B,Skv,Hkv,D] for k and
+ * v, D contiguous) of bf16 or, with f16 = 1, IEEE binary16 (the Pallas page
+ * accepts both), widened exactly to fp64.  Nothing is blocked, fused or
  * reordered: each row is two passes over its keys (max, then sums).
  *
  * The partial-triple entry point returns the un-normalised (m, l, o) of a row
@@ -48,12 +49,30 @@ static double widen_bf16(uint16_t bits) {
     return (double)f;
 }
 
+/* IEEE binary16: sign, 5-bit exponent (bias 15), 10-bit fraction; exact in fp64 */
+static double widen_f16(uint16_t bits) {
+    const int sign = bits >> 15, e = (bits >> 10) & 0x1F, frac = bits & 0x3FF;
+    double mag;
+    if (e == 0)
+        mag = ldexp((double)frac, -24); /* zero and subnormals */
+    else if (e == 31)
+        mag = frac ? NAN : INFINITY;
+    else
+        mag = ldexp((double)(1024 + frac), e - 25);
+    return sign ? -mag : mag;
+}
+
 typedef struct {
     const uint16_t *q, *k, *v;
     long B, Sq, Skv, Hq, Hkv, D;
     int causal;
     double scale;
+    int f16; /* element format of q, k, v: 0 bf16, 1 IEEE binary16 */
 } problem_t;
+
+static double widen(const problem_t *p, uint16_t bits) {
+    return p->f16 ? widen_f16(bits) : widen_bf16(bits);
+}
 
 /* last visible key index + 1 for query row i (may be <= 0: no visible key) */
 static long visible_end(const problem_t *p, long i) {
@@ -78,14 +97,14 @@ static void row_triple(const problem_t *p, long b, long h, long i, long j_lo, lo
         return;
     }
     const uint16_t *qrow = p->q + ((b * p->Sq + i) * p->Hq + h) * D;
-    for (long d = 0; d < D; ++d) qd[d] = widen_bf16(qrow[d]);
+    for (long d = 0; d < D; ++d) qd[d] = widen(p, qrow[d]);
 
     /* pass 1: scaled logits and their maximum */
     double m = -INFINITY;
     for (long j = j_lo; j < end; ++j) {
         const uint16_t *krow = p->k + ((b * p->Skv + j) * p->Hkv + g) * D;
         double acc = 0.0;
-        for (long d = 0; d < D; ++d) acc += qd[d] * widen_bf16(krow[d]);
+        for (long d = 0; d < D; ++d) acc += qd[d] * widen(p, krow[d]);
         double s = p->scale * acc;
         s_buf[j - j_lo] = s;
         if (s > m) m = s;
@@ -96,7 +115,7 @@ static void row_triple(const problem_t *p, long b, long h, long i, long j_lo, lo
         double w = exp(s_buf[j - j_lo] - m);
         l += w;
         const uint16_t *vrow = p->v + ((b * p->Skv + j) * p->Hkv + g) * D;
-        for (long d = 0; d < D; ++d) o_out[d] += w * widen_bf16(vrow[d]);
+        for (long d = 0; d < D; ++d) o_out[d] += w * widen(p, vrow[d]);
     }
     *m_out = m;
     *l_out = l;
@@ -114,10 +133,10 @@ static int check_dims(long B, long Sq, long Skv, long Hq, long Hkv, long D) {
  * lse_out: nrows doubles.  Returns 0, or -1 on bad arguments.
  */
 int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, long B, long Sq,
-                     long Skv, long Hq, long Hkv, long D, int causal, double scale, long nrows,
-                     const long *rows, double *o_out, double *lse_out) {
+                     long Skv, long Hq, long Hkv, long D, int causal, double scale, int f16,
+                     long nrows, const long *rows, double *o_out, double *lse_out) {
     if (check_dims(B, Sq, Skv, Hq, Hkv, D) || causal < 0 || causal > 2) return -1;
-    problem_t p = {q, k, v, B, Sq, Skv, Hq, Hkv, D, causal, scale};
+    problem_t p = {q, k, v, B, Sq, Skv, Hq, Hkv, D, causal, scale, f16 != 0};
     for (long r = 0; r < nrows; ++r) {
         const long *t = rows + 3 * r;
         if (t[0] < 0 || t[0] >= B || t[1] < 0 || t[1] >= Hq || t[2] < 0 || t[2] >= Sq)
@@ -156,10 +175,10 @@ int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, lo
  * Attention output for every row.  o_out: [B,Sq,Hq,D] doubles; lse_out: [B,Hq,Sq].
  */
 int oracle_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, long B, long Sq,
-                    long Skv, long Hq, long Hkv, long D, int causal, double scale,
+                    long Skv, long Hq, long Hkv, long D, int causal, double scale, int f16,
                     double *o_out, double *lse_out) {
     if (check_dims(B, Sq, Skv, Hq, Hkv, D) || causal < 0 || causal > 2) return -1;
-    problem_t p = {q, k, v, B, Sq, Skv, Hq, Hkv, D, causal, scale};
+    problem_t p = {q, k, v, B, Sq, Skv, Hq, Hkv, D, causal, scale, f16 != 0};
     const long nrows = B * Hq * Sq;
     int bad = 0;
 #pragma omp parallel
@@ -197,12 +216,12 @@ int oracle_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, lon
  */
 int oracle_partial_triple(const uint16_t *q, const uint16_t *k, const uint16_t *v, long B,
                           long Sq, long Skv, long Hq, long Hkv, long D, int causal,
-                          double scale, long b, long h, long i, long j_lo, long j_hi,
+                          double scale, int f16, long b, long h, long i, long j_lo, long j_hi,
                           double *m_out, double *l_out, double *o_out) {
     if (check_dims(B, Sq, Skv, Hq, Hkv, D) || causal < 0 || causal > 2) return -1;
     if (b < 0 || b >= B || h < 0 || h >= Hq || i < 0 || i >= Sq) return -1;
     if (j_lo < 0 || j_hi > Skv || j_lo > j_hi) return -1;
-    problem_t p = {q, k, v, B, Sq, Skv, Hq, Hkv, D, causal, scale};
+    problem_t p = {q, k, v, B, Sq, Skv, Hq, Hkv, D, causal, scale, f16 != 0};
     double *s_buf = (double *)malloc(sizeof(double) * (size_t)(j_hi - j_lo + 1));
     double *qd = (double *)malloc(sizeof(double) * (size_t)D);
     int rc = 0;

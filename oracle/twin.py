@@ -13,14 +13,16 @@ from __future__ import annotations
 import numpy as np
 
 
-def _widen(bits):
-    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(
-        np.float64)
+def _widen(bits, f16=False):
+    bits = np.asarray(bits, dtype=np.uint16)
+    if f16:  # numpy's own binary16 type
+        return bits.view(np.float16).astype(np.float64)
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-def attention(q_bits, k_bits, v_bits, causal: int, scale: float):
-    """Returns (o [B,Sq,Hq,D] fp64, lse [B,Hq,Sq] fp64)."""
-    q, k, v = _widen(q_bits), _widen(k_bits), _widen(v_bits)
+def attention(q_bits, k_bits, v_bits, causal: int, scale: float, f16: bool = False):
+    """Returns (o [B,Sq,Hq,D] fp64, lse [B,Hq,Sq] fp64); f16: binary16 inputs."""
+    q, k, v = _widen(q_bits, f16), _widen(k_bits, f16), _widen(v_bits, f16)
     B, Sq, Hq, D = q.shape
     Skv, Hkv = k.shape[1], k.shape[2]
     group = Hq // Hkv

@@ -119,3 +119,23 @@ def test_splitkv_workspace_size_argument_checks(lib):
     with pytest.raises(fa.AttnError) as e:
         fa.attn_fwd_splitkv_workspace_size(1, 256, 256, 3, 2, 128, 1)
     assert e.value.status == fa.ATTN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("dtype", [-1, 2, 7])
+def test_fwd_ex_rejects_unknown_dtype(lib, dtype):
+    a = GOOD
+    assert fa.attn_fwd_ex_ptr(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Sq"], a["Skv"],
+                              a["Hq"], a["Hkv"], a["D"], a["causal"], a["scale"], dtype,
+                              0) == fa.ATTN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("dtype", [0, 1])
+def test_fwd_ex_validates_like_attn_fwd(lib, dtype):
+    a = {**GOOD, "q": 0}
+    assert fa.attn_fwd_ex_ptr(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Sq"], a["Skv"],
+                              a["Hq"], a["Hkv"], a["D"], a["causal"], a["scale"], dtype,
+                              0) == fa.ATTN_ERR_INVALID_ARG
+    a = {**GOOD, "D": 64}
+    assert fa.attn_fwd_ex_ptr(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Sq"], a["Skv"],
+                              a["Hq"], a["Hkv"], a["D"], a["causal"], a["scale"], dtype,
+                              0) == fa.ATTN_ERR_UNSUPPORTED

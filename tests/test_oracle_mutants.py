@@ -33,6 +33,12 @@ MUTANTS = [
     ("v_by_query_row", "const uint16_t *vrow = p->v + ((b * p->Skv + j) * p->Hkv + g) * D;",
      "const uint16_t *vrow = p->v + ((b * p->Skv + (i < p->Skv ? i : j)) * p->Hkv + g) * D;"),
     ("sign_flip", "double s = p->scale * acc;", "double s = -p->scale * acc;"),
+    ("f16_read_as_bf16", "return p->f16 ? widen_f16(bits) : widen_bf16(bits);",
+     "return widen_bf16(bits);"),
+    ("f16_exponent_bias", "mag = ldexp((double)(1024 + frac), e - 25);",
+     "mag = ldexp((double)(1024 + frac), e - 24);"),
+    ("f16_subnormal_scale", "mag = ldexp((double)frac, -24); /* zero and subnormals */",
+     "mag = ldexp((double)frac, -25);"),
 ]
 
 PIN_TESTS = [
@@ -41,6 +47,7 @@ PIN_TESTS = [
     "test_brute_force_twin", "test_gqa_head_repeat_equivalence",
     "test_bottom_right_equals_tail_of_square_causal", "test_shift_invariance_large_logits",
     "test_merge_identity_random_chunks", "test_top_left_rules",
+    "test_f16_widening_every_finite_pattern", "test_f16_brute_force_twin",
 ]
 
 

@@ -353,3 +353,48 @@ def test_top_left_rules():
     kk, vv = np.ascontiguousarray(k[:, :9]), np.ascontiguousarray(v[:, :9])
     o_sq, l_sq = oracle.attn_full(q, kk, vv, 1, 0.09)
     assert np.array_equal(o_tl, o_sq) and np.array_equal(l_tl, l_sq)
+
+
+# --------------------------------------------------------------------------- binary16 inputs
+
+
+def test_f16_widening_every_finite_pattern():
+    """Q = K = 0 and one key: o equals that key's V row exactly, so the oracle's
+    own binary16 widening is checked against numpy's float16 for every finite
+    bit pattern (both zeros, subnormals, normals up to 65504)."""
+    bits = np.arange(65536, dtype=np.uint16)
+    finite = np.isfinite(bits.view(np.float16))
+    vrow = bits[finite]
+    D = vrow.size
+    q = np.zeros((1, 1, 1, D), dtype=np.uint16)
+    k = np.zeros((1, 1, 1, D), dtype=np.uint16)
+    v = np.ascontiguousarray(vrow.reshape(1, 1, 1, D))
+    o, lse = oracle.attn_full(q, k, v, 0, 1.0, f16=True)
+    want = vrow.view(np.float16).astype(np.float64)
+    assert np.array_equal(o[0, 0, 0], want) and lse[0, 0, 0] == 0.0
+    assert np.array_equal(oracle.f16_bits_to_f64(vrow), want)
+
+
+def test_round_f16_matches_numpy():
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal(200_000) * np.exp(rng.uniform(-22, 12, 200_000))
+    half = np.ldexp(1.0, -11)   # ties: 1 + (2k+1) 2^-11 in [1, 2)
+    ties = 1.0 + (2 * rng.integers(0, 1024, 1000) + 1) * half
+    x = np.concatenate([x, ties, -ties, [65504.0, 65519.9, 65520.0, 2.0 ** -25, 3 * 2.0 ** -26]])
+    with np.errstate(over="ignore"):  # 65520 rounds up past the largest finite value
+        want = x.astype(np.float16).astype(np.float64)
+    assert np.array_equal(oracle.round_f16(x), want)
+
+
+@pytest.mark.parametrize("causal", [0, 1, 2])
+def test_f16_brute_force_twin(causal):
+    B, Sq, Skv, Hq, Hkv, D = 1, 37, 50, 4, 2, 128
+    q, k, v = inputs.make_qkv(B, Sq, Skv, Hq, Hkv, D, seed=41, q_sigma=3.0, dtype="f16")
+    o1, l1 = oracle.attn_full(q, k, v, causal, 0.0884, f16=True)
+    o2, l2 = twin.attention(q, k, v, causal, 0.0884, f16=True)
+    fin = np.isfinite(l1)
+    assert np.array_equal(fin, np.isfinite(l2))
+    assert np.max(np.abs(o1 - o2)) < 1e-12 and np.max(np.abs(l1[fin] - l2[fin])) < 1e-12
+    # the same bits read as bf16 give a different problem: the format flag matters
+    o3, _ = oracle.attn_full(q, k, v, causal, 0.0884)
+    assert not np.allclose(o1, o3)
