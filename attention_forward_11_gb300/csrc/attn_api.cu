@@ -61,6 +61,12 @@ bool encode_bshd(CUtensorMap* map, const void* ptr, int B, int S, int H, int D, 
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <class Sched, bool kF16, int kD>
+bool opt_in_smem() {
+    return cudaFuncSetAttribute(attn::fmha_fwd_kernel<Sched, kF16, kD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                attn::Geo<kD>::kSmemBytes) == cudaSuccess;
+}
+
 // Per-device one-time set-up: the kernels' shared-memory opt-in and the SM count.
 bool device_setup(int dev, int* sm_count) {
     static std::mutex mu;
@@ -69,12 +75,9 @@ bool device_setup(int dev, int* sm_count) {
     std::lock_guard<std::mutex> lock(mu);
     if (sms[dev] == 0) {
         int n = 0;
-        if (cudaFuncSetAttribute(attn::fmha_fwd_kernel<attn::PlainSched, false>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, attn::kSmemBytes) != cudaSuccess ||
-            cudaFuncSetAttribute(attn::fmha_fwd_kernel<attn::PlainSched, true>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, attn::kSmemBytes) != cudaSuccess ||
-            cudaFuncSetAttribute(attn::fmha_fwd_kernel<attn::SplitSched, false>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, attn::kSmemBytes) != cudaSuccess ||
+        if (!opt_in_smem<attn::PlainSched, false, 128>() || !opt_in_smem<attn::PlainSched, true, 128>() ||
+            !opt_in_smem<attn::SplitSched, false, 128>() || !opt_in_smem<attn::PlainSched, false, 64>() ||
+            !opt_in_smem<attn::PlainSched, true, 64>() || !opt_in_smem<attn::SplitSched, false, 64>() ||
             cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
             return false;
         sms[dev] = n;
@@ -94,7 +97,7 @@ attn_status_t check_sizes(int B, int Sq, int Skv, int Hq, int Hkv, int D, int ca
     if (B < 1 || Sq < 1 || Skv < 1 || Hq < 1 || Hkv < 1 || D < 1) return ATTN_ERR_INVALID_ARG;
     if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
     if (causal < 0 || causal > 2) return ATTN_ERR_INVALID_ARG;
-    if (D != attn::kHeadDim) return ATTN_ERR_UNSUPPORTED;
+    if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
     return ATTN_OK;
 }
 
@@ -118,7 +121,7 @@ attn_status_t check_pointers(const void* q, const void* k, const void* v, const 
 
 // Work decomposition: two 128-row query tiles per unit sharing one K/V head.
 attn_status_t make_params(int B, int Sq, int Skv, int Hq, int Hkv, int causal, float scale, void* o,
-                          float* lse, attn::FwdParams* out) {
+                          float* lse, attn::FwdParams* out, int D = 128) {
     if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
     attn::FwdParams p{};
     p.B = B;
@@ -126,6 +129,7 @@ attn_status_t make_params(int B, int Sq, int Skv, int Hq, int Hkv, int causal, f
     p.Skv = Skv;
     p.Hq = Hq;
     p.Hkv = Hkv;
+    p.D = D;
     p.causal = causal;
     p.diag = causal == 1 ? Skv - Sq : 0;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
@@ -164,8 +168,8 @@ struct SplitPlan {
 };
 constexpr size_t kWorkspaceAlign = 256;
 
-size_t workspace_bytes_for(int n_slots) {
-    const size_t o_bytes = (size_t)n_slots * attn::kTiles * attn::kBM * attn::kHeadDim * sizeof(float);
+size_t workspace_bytes_for(int n_slots, int D) {
+    const size_t o_bytes = (size_t)n_slots * attn::kTiles * attn::kBM * D * sizeof(float);
     const size_t ml_bytes = (size_t)n_slots * attn::kTiles * attn::kBM * sizeof(float2);
     const size_t o_pad = (o_bytes + kWorkspaceAlign - 1) / kWorkspaceAlign * kWorkspaceAlign;
     return o_pad + ml_bytes;
@@ -237,8 +241,14 @@ template <bool kF16 = false>
 attn_status_t launch_plain(const CUtensorMap* tm, const attn::FwdParams& p, int sms, cudaStream_t stream) {
     // persistent grid: at most one CTA per SM (the CTA holds all 512 TMEM columns)
     const int grid = p.n_units < sms ? p.n_units : sms;
-    attn::fmha_fwd_kernel<attn::PlainSched, kF16><<<static_cast<unsigned int>(grid), attn::kThreads, attn::kSmemBytes,
-                                              stream>>>(tm[0], tm[1], tm[2], tm[3], p, attn::PlainSched{0});
+    if (p.D == 64)
+        attn::fmha_fwd_kernel<attn::PlainSched, kF16, 64><<<static_cast<unsigned int>(grid), attn::kThreads,
+                                                            attn::Geo<64>::kSmemBytes, stream>>>(
+            tm[0], tm[1], tm[2], tm[3], p, attn::PlainSched{0});
+    else
+        attn::fmha_fwd_kernel<attn::PlainSched, kF16, 128><<<static_cast<unsigned int>(grid), attn::kThreads,
+                                                             attn::Geo<128>::kSmemBytes, stream>>>(
+            tm[0], tm[1], tm[2], tm[3], p, attn::PlainSched{0});
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return ATTN_OK;
@@ -246,12 +256,18 @@ attn_status_t launch_plain(const CUtensorMap* tm, const attn::FwdParams& p, int 
 
 attn_status_t launch_split(const CUtensorMap* tm, const attn::FwdParams& p, SplitPlan& plan, void* workspace,
                            cudaStream_t stream) {
-    const size_t o_bytes = (size_t)plan.n_slots * attn::kTiles * attn::kBM * attn::kHeadDim * sizeof(float);
+    const size_t o_bytes = (size_t)plan.n_slots * attn::kTiles * attn::kBM * p.D * sizeof(float);
     const size_t o_pad = (o_bytes + kWorkspaceAlign - 1) / kWorkspaceAlign * kWorkspaceAlign;
     plan.sched.ws_o = static_cast<float*>(workspace);
     plan.sched.ws_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) + o_pad);
-    attn::fmha_fwd_kernel<attn::SplitSched, false><<<static_cast<unsigned int>(plan.grid), attn::kThreads,
-                                              attn::kSmemBytes, stream>>>(tm[0], tm[1], tm[2], tm[3], p, plan.sched);
+    if (p.D == 64)
+        attn::fmha_fwd_kernel<attn::SplitSched, false, 64><<<static_cast<unsigned int>(plan.grid), attn::kThreads,
+                                                             attn::Geo<64>::kSmemBytes, stream>>>(
+            tm[0], tm[1], tm[2], tm[3], p, plan.sched);
+    else
+        attn::fmha_fwd_kernel<attn::SplitSched, false, 128><<<static_cast<unsigned int>(plan.grid), attn::kThreads,
+                                                              attn::Geo<128>::kSmemBytes, stream>>>(
+            tm[0], tm[1], tm[2], tm[3], p, plan.sched);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);
     plan.comb.ws_o = plan.sched.ws_o;
@@ -259,7 +275,10 @@ attn_status_t launch_split(const CUtensorMap* tm, const attn::FwdParams& p, Spli
     plan.comb.o = p.o;
     const long long warps = (long long)plan.comb.n * attn::kTiles * attn::kBM;
     const unsigned int blocks = static_cast<unsigned int>((warps + attn::kCombineWarps - 1) / attn::kCombineWarps);
-    attn::splitkv_combine_kernel<false><<<blocks, 32 * attn::kCombineWarps, 0, stream>>>(p, plan.comb);
+    if (p.D == 64)
+        attn::splitkv_combine_kernel<false, 64><<<blocks, 32 * attn::kCombineWarps, 0, stream>>>(p, plan.comb);
+    else
+        attn::splitkv_combine_kernel<false, 128><<<blocks, 32 * attn::kCombineWarps, 0, stream>>>(p, plan.comb);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return ATTN_OK;
@@ -278,7 +297,7 @@ attn_status_t fwd_impl(const void* q, const void* k, const void* v, void* o, flo
     const attn_status_t sp = check_pointers(q, k, v, o, lse, B, Sq, Skv, Hq, Hkv, D > 0 ? D : 1);
     if (sp != ATTN_OK) return sp;
     attn::FwdParams p{};
-    const attn_status_t sm = make_params(B, Sq, Skv, Hq, Hkv, causal, scale, o, lse, &p);
+    const attn_status_t sm = make_params(B, Sq, Skv, Hq, Hkv, causal, scale, o, lse, &p, D);
     if (sm != ATTN_OK) return sm;
     if (st != ATTN_OK) return st;  // valid request, unsupported head size
     CUtensorMap tm[4];
@@ -310,13 +329,13 @@ extern "C" attn_status_t attn_fwd_splitkv_workspace_size(int B, int Sq, int Skv,
     const attn_status_t st = check_sizes(B, Sq, Skv, Hq, Hkv, D, causal);
     if (st != ATTN_OK) return st;
     attn::FwdParams p{};
-    const attn_status_t sm = make_params(B, Sq, Skv, Hq, Hkv, causal, 1.0f, nullptr, nullptr, &p);
+    const attn_status_t sm = make_params(B, Sq, Skv, Hq, Hkv, causal, 1.0f, nullptr, nullptr, &p, D);
     if (sm != ATTN_OK) return sm;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || !device_setup(dev, &sms)) return ATTN_ERR_CUDA;
     std::unique_ptr<SplitPlan> plan(new SplitPlan());
     build_split_plan(p, sms, plan.get());
-    *bytes = plan->split ? workspace_bytes_for(plan->n_slots) : 0;
+    *bytes = plan->split ? workspace_bytes_for(plan->n_slots, D) : 0;
     return ATTN_OK;
 }
 
@@ -330,7 +349,7 @@ extern "C" attn_status_t attn_fwd_splitkv(const void* q, const void* k, const vo
     if (sp != ATTN_OK) return sp;
     if (workspace && reinterpret_cast<uintptr_t>(workspace) % kWorkspaceAlign != 0) return ATTN_ERR_INVALID_ARG;
     attn::FwdParams p{};
-    const attn_status_t sm = make_params(B, Sq, Skv, Hq, Hkv, causal, scale, o, lse, &p);
+    const attn_status_t sm = make_params(B, Sq, Skv, Hq, Hkv, causal, scale, o, lse, &p, D);
     if (sm != ATTN_OK) return sm;
     if (st != ATTN_OK) return st;
     int dev = 0, sms = 0;
@@ -338,7 +357,7 @@ extern "C" attn_status_t attn_fwd_splitkv(const void* q, const void* k, const vo
     std::unique_ptr<SplitPlan> plan(new SplitPlan());
     build_split_plan(p, sms, plan.get());
     if (plan->split) {
-        const size_t need = workspace_bytes_for(plan->n_slots);
+        const size_t need = workspace_bytes_for(plan->n_slots, D);
         if (!workspace || workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
         const size_t q_bytes = (size_t)B * Sq * Hq * D * 2, kv_bytes = (size_t)B * Skv * Hkv * D * 2;
         if (ranges_overlap(workspace, need, q, q_bytes) || ranges_overlap(workspace, need, k, kv_bytes) ||
@@ -451,7 +470,7 @@ extern "C" attn_status_t attn_fwd_splitkv_noalloc(const void* q, const void* k, 
     const attn_status_t sp = check_pointers(q, k, v, o, lse, B, Sq, Skv, Hq, Hkv, D > 0 ? D : 1);
     if (sp != ATTN_OK) return sp;
     attn::FwdParams p{};
-    const attn_status_t sm = make_params(B, Sq, Skv, Hq, Hkv, causal, scale, o, lse, &p);
+    const attn_status_t sm = make_params(B, Sq, Skv, Hq, Hkv, causal, scale, o, lse, &p, D);
     if (sm != ATTN_OK) return sm;
     if (st != ATTN_OK) return st;
     int dev = 0, sms = 0;
@@ -463,7 +482,7 @@ extern "C" attn_status_t attn_fwd_splitkv_noalloc(const void* q, const void* k, 
     static SplitPlan plan;
     std::lock_guard<std::mutex> lock(plan_mu);
     build_split_plan_fixed(p, sms, &plan);
-    if (plan.split && workspace_bytes_for(plan.n_slots) > kStaticScratchBytes) return ATTN_ERR_UNSUPPORTED;
+    if (plan.split && workspace_bytes_for(plan.n_slots, D) > kStaticScratchBytes) return ATTN_ERR_UNSUPPORTED;
     CUtensorMap tm[4];
     if (!encode_maps(q, k, v, o, B, Sq, Skv, Hq, Hkv, D, tm)) return ATTN_ERR_CUDA;
     return plan.split ? launch_split(tm, p, plan, scratch, stream) : launch_plain(tm, p, sms, stream);

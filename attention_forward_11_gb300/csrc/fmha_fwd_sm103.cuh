@@ -65,12 +65,10 @@ namespace attn {
 
 constexpr int kBM = 128;                 // query rows per tile (= TMEM lanes)
 constexpr int kBN = 128;                 // keys per KV tile
-constexpr int kHeadDim = 128;            // D
 constexpr int kTiles = 2;                // query tiles per unit
 constexpr int kKStages = ATTN_KSTAGES;   // K ring depth
 constexpr int kVStages = ATTN_VSTAGES;   // V ring depth
-constexpr int kTileBytes = kBM * kHeadDim * 2;   // 32 KB bf16 tile (Q, K or V)
-constexpr int kHalfBytes = kTileBytes / 2;       // one 64-column, 128-byte-swizzled half
+constexpr int kHalfBytes = kBM * 64 * 2;         // 128 rows x one 64-column, 128-byte-swizzled half
 constexpr int kSoftmaxWarps = 4 * kTiles;          // warpgroups 0 and 1
 constexpr int kEpilogueWarp0 = kSoftmaxWarps;      // warpgroup 2
 constexpr int kMmaWarp = kEpilogueWarp0 + 4;       // warpgroup 3
@@ -84,13 +82,6 @@ constexpr uint32_t kTmemS = 0;           // S_t at kTmemS + 128 t
 constexpr uint32_t kTmemO = 256;         // O_t at kTmemO + 128 t
 constexpr float kRescaleLog2 = 8.0f;     // raise the running max only past 2^8
 
-// shared memory map (offsets from a 1024-byte aligned base)
-constexpr int kSmemQ = 0;
-constexpr int kSmemK = kSmemQ + kTiles * kTileBytes;
-constexpr int kSmemV = kSmemK + kKStages * kTileBytes;
-constexpr int kSmemStage = kSmemV + kVStages * kTileBytes;  // O staging: one 64-column half
-constexpr int kSmemStats = kSmemStage + kHalfBytes;           // per tile and row: (m, l)
-constexpr int kSmemBar = kSmemStats + kTiles * kBM * 8;
 enum : int {
     BAR_QFULL = 0,
     BAR_QEMPTY = BAR_QFULL + kTiles,
@@ -107,11 +98,26 @@ enum : int {
     BAR_MMADONE = BAR_STATSFREE + kTiles,
     BAR_COUNT
 };
-constexpr int kSmemTmemSlot = kSmemBar + BAR_COUNT * 8;
-constexpr int kSmemAbort = kSmemTmemSlot + 4;
-constexpr int kSmemUsed = kSmemAbort + 4;
-constexpr int kSmemBytes = kSmemUsed + 1024;  // + slack to align the base to 1024 bytes
-static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
+// Shared-memory map for head size kD (offsets from a 1024-byte aligned base).
+// Every row of a Q, K or V tile is kD / 64 halves of 64 columns, each half a
+// 128-row x 128-byte block in the 128-byte swizzle (TMA box and UMMA atom).
+template <int kD>
+struct Geo {
+    static_assert(kD == 64 || kD == 128, "head size 64 or 128");
+    static constexpr int kHalves = kD / 64;
+    static constexpr int kTileBytes = kBM * kD * 2;  // Q, K or V tile
+    static constexpr int kSmemQ = 0;
+    static constexpr int kSmemK = kSmemQ + kTiles * kTileBytes;
+    static constexpr int kSmemV = kSmemK + kKStages * kTileBytes;
+    static constexpr int kSmemStage = kSmemV + kVStages * kTileBytes;  // O staging: one half
+    static constexpr int kSmemStats = kSmemStage + kHalfBytes;         // per tile and row: (m, l)
+    static constexpr int kSmemBar = kSmemStats + kTiles * kBM * 8;
+    static constexpr int kSmemTmemSlot = kSmemBar + BAR_COUNT * 8;
+    static constexpr int kSmemAbort = kSmemTmemSlot + 4;
+    static constexpr int kSmemUsed = kSmemAbort + 4;
+    static constexpr int kSmemBytes = kSmemUsed + 1024;  // + slack to align the base to 1024 bytes
+    static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
+};
 
 constexpr unsigned int kStatusTimeout = 1u;
 
@@ -120,6 +126,7 @@ __device__ unsigned int g_attn_status = 0;
 
 struct FwdParams {
     int B, Sq, Skv, Hq, Hkv;
+    int D;                  // head size (64 or 128); selects the kernel instance
     int causal;             // 0: none; 1: bottom-right; 2: top-left
     int diag;               // key j visible from row i iff j <= i + diag (when causal)
     float scale_log2;       // softmax scale * log2(e)
@@ -281,20 +288,22 @@ __device__ __forceinline__ bool get_work(const FwdParams& p, const SplitSched& s
 }
 
 // kF16: Q, K, V, O are IEEE binary16 instead of bf16 (P follows the operands).
-template <class Sched, bool kF16>
+// kD: head size (64 or 128).
+template <class Sched, bool kF16, int kD>
 __global__ void __launch_bounds__(kThreads, 1)
     fmha_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                     const FwdParams p, const __grid_constant__ Sched sched) {
+    using G = Geo<kD>;
     extern __shared__ uint8_t smem_raw[];
     // align in the shared window (swizzle atoms and TMA boxes want 1024 bytes)
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(smem);
     const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) / 32, 0);
     const int lane = static_cast<int>(threadIdx.x) & 31;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmemAbort);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kSmemTmemSlot);
-    auto bar = [&](int i) -> uint32_t { return sbase + kSmemBar + 8 * i; };
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + G::kSmemAbort);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::kSmemTmemSlot);
+    auto bar = [&](int i) -> uint32_t { return sbase + G::kSmemBar + 8 * i; };
 
     // ---- set-up: barriers, abort flag, tensor memory
     if (warp == kLoadWarp && lane == 0) {
@@ -355,9 +364,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(bar(BAR_QFULL + t), kTileBytes);
-                    for (int h = 0; h < 2; ++h)
-                        tma_load_4d(sbase + kSmemQ + t * kTileBytes + h * kHalfBytes, &tm_q, h * 64,
+                    mbar_arrive_expect_tx(bar(BAR_QFULL + t), G::kTileBytes);
+                    for (int h = 0; h < G::kHalves; ++h)
+                        tma_load_4d(sbase + G::kSmemQ + t * G::kTileBytes + h * kHalfBytes, &tm_q, h * 64,
                                     w.hq(t), w.row(t), w.b, bar(BAR_QFULL + t), pol_q);
                     ++q_issued[t];
                 }
@@ -365,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 Unit wn;
                 if (get_work(p, sched, j + 1, wn)) {  // warm L2 with the next unit's Q meanwhile
                     for (int t = 0; t < kTiles; ++t)
-                        for (int h = 0; h < 2; ++h) tma_prefetch_l2_4d(&tm_q, h * 64, wn.hq(t), wn.row(t), wn.b);
+                        for (int h = 0; h < G::kHalves; ++h) tma_prefetch_l2_4d(&tm_q, h * 64, wn.hq(t), wn.row(t), wn.b);
                 }
                 const int nm = w.nmax();
                 for (int kt = 0; kt < nm; ++kt) {
@@ -374,9 +383,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(bar(BAR_KFULL + ks), kTileBytes);
-                    for (int h = 0; h < 2; ++h)
-                        tma_load_4d(sbase + kSmemK + ks * kTileBytes + h * kHalfBytes, &tm_k, h * 64,
+                    mbar_arrive_expect_tx(bar(BAR_KFULL + ks), G::kTileBytes);
+                    for (int h = 0; h < G::kHalves; ++h)
+                        tma_load_4d(sbase + G::kSmemK + ks * G::kTileBytes + h * kHalfBytes, &tm_k, h * 64,
                                     w.hkv, (w.kb + kt) * kBN, w.b, bar(BAR_KFULL + ks), pol_kv);
                     ++k_issued;
                     const int vs = v_issued % kVStages, vuse = v_issued / kVStages;
@@ -384,9 +393,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(bar(BAR_VFULL + vs), kTileBytes);
-                    for (int h = 0; h < 2; ++h)
-                        tma_load_4d(sbase + kSmemV + vs * kTileBytes + h * kHalfBytes, &tm_v, h * 64,
+                    mbar_arrive_expect_tx(bar(BAR_VFULL + vs), G::kTileBytes);
+                    for (int h = 0; h < G::kHalves; ++h)
+                        tma_load_4d(sbase + G::kSmemV + vs * G::kTileBytes + h * kHalfBytes, &tm_v, h * 64,
                                     w.hkv, (w.kb + kt) * kBN, w.b, bar(BAR_VFULL + vs), pol_kv);
                     ++v_issued;
                 }
@@ -409,17 +418,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The whole warp runs the control flow (so descriptors and stage indices stay
         // warp-uniform); one elected lane issues each group of MMAs and its commits.
         constexpr uint32_t idesc_qk = idesc_f16kind_f32(kBM, kBN, false, kF16);
-        constexpr uint32_t idesc_pv = idesc_f16kind_f32(kBM, kHeadDim, true, kF16);
+        constexpr uint32_t idesc_pv = idesc_f16kind_f32(kBM, kD, true, kF16);
         // descriptor of k-step kk = base descriptor + constant start-address offset (>> 4)
-        const uint64_t q_desc0 = sdesc_sw128(sbase + kSmemQ, 16, 1024);
-        const uint64_t k_desc0 = sdesc_sw128(sbase + kSmemK, 16, 1024);
-        const uint64_t v_desc0 = sdesc_sw128(sbase + kSmemV, kHalfBytes, 1024);
+        const uint64_t q_desc0 = sdesc_sw128(sbase + G::kSmemQ, 16, 1024);
+        const uint64_t k_desc0 = sdesc_sw128(sbase + G::kSmemK, 16, 1024);
+        const uint64_t v_desc0 = sdesc_sw128(sbase + G::kSmemV, kHalfBytes, 1024);
         auto issue_qk = [&](int t, int ks) {
             const uint32_t d = tmem_base + kTmemS + 128 * t;
-            const uint64_t qd = q_desc0 + static_cast<uint64_t>((t * kTileBytes) >> 4);
-            const uint64_t kd = k_desc0 + static_cast<uint64_t>((ks * kTileBytes) >> 4);
+            const uint64_t qd = q_desc0 + static_cast<uint64_t>((t * G::kTileBytes) >> 4);
+            const uint64_t kd = k_desc0 + static_cast<uint64_t>((ks * G::kTileBytes) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+            for (int kk = 0; kk < kD / 16; ++kk) {
                 const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
                 mma_bf16_ss(d, qd + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
             }
@@ -428,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto issue_pv = [&](int t, int vs, int h, bool accumulate) {
             const uint32_t d = tmem_base + kTmemO + 128 * t;
             const uint32_t pa = tmem_base + kTmemS + 128 * t;
-            const uint64_t vd = v_desc0 + static_cast<uint64_t>((vs * kTileBytes) >> 4);
+            const uint64_t vd = v_desc0 + static_cast<uint64_t>((vs * G::kTileBytes) >> 4);
 #pragma unroll
             for (int q = 0; q < kBN / 32; ++q) {
                 const int kk = h * (kBN / 32) + q;
@@ -631,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool need = (kt > 0) && (alpha != 1.f);
                 if (__any_sync(0xffffffffu, need)) {
 #pragma unroll 1
-                    for (int c = 0; c < 8; ++c) {
+                    for (int c = 0; c < kD / 16; ++c) {
                         uint32_t o[16];
                         tmem_ld16(tO + 16 * c, o);
                         tmem_wait_ld_regs16(o);
@@ -689,7 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = false;
                 break;
             }
-            reinterpret_cast<float2*>(smem + kSmemStats)[t * kBM + r] = make_float2(m_run, l_run);
+            reinterpret_cast<float2*>(smem + G::kSmemStats)[t * kBM + r] = make_float2(m_run, l_run);
             mbar_arrive(bar(BAR_STATSFULL + t));
         }
     } else if (wg == 2) {
@@ -698,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int wq = warp % 4;
         const int r = wq * 32 + lane;  // row within a tile = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-        uint8_t* stage = smem + kSmemStage;
+        uint8_t* stage = smem + G::kSmemStage;
         bool ok = true;
         for (int j = 0; ok; ++j) {
             Unit w;
@@ -712,7 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const float2 ml = reinterpret_cast<const float2*>(smem + kSmemStats)[t * kBM + r];
+                const float2 ml = reinterpret_cast<const float2*>(smem + G::kSmemStats)[t * kBM + r];
                 mbar_arrive(bar(BAR_STATSFREE + t));
                 const float m_run = ml.x, l_run = ml.y;
                 const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
@@ -725,9 +734,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // a piece of a split unit: the raw fp32 accumulator and (m, l) of
                         // every row go to its workspace slot for the combine kernel
                         const size_t rr = (static_cast<size_t>(w.slot) * kTiles + t) * kBM + r;
-                        uint4* dst = reinterpret_cast<uint4*>(sched.ws_o + rr * kHeadDim);
+                        uint4* dst = reinterpret_cast<uint4*>(sched.ws_o + rr * kD);
 #pragma unroll
-                        for (int h = 0; h < 2; ++h) {
+                        for (int h = 0; h < G::kHalves; ++h) {
                             uint32_t o[64];
                             if (nt > 0) {
                                 tmem_ld32(tO + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
@@ -738,7 +747,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                                 for (int e = 0; e < 64; ++e) o[e] = 0u;
                             }
-                            if (h == 1) {  // O_t may now be overwritten by the next item's first P.V
+                            if (h == G::kHalves - 1) {  // O_t may now be overwritten by the next item's first P.V
                                 tc_fence_before();
                                 mbar_arrive(bar(BAR_OFREE + t));
                             }
@@ -753,7 +762,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // two 64-column halves: TMEM -> registers -> (1/l) -> bf16 -> swizzled
                 // staging -> one TMA store each (rows past Sq are clipped by the store)
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
+                for (int h = 0; h < G::kHalves; ++h) {
                     uint32_t o[64];
                     if (nt > 0) {
                         tmem_ld32(tO + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
@@ -764,7 +773,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int e = 0; e < 64; ++e) o[e] = 0u;
                     }
-                    if (h == 1) {  // O_t may now be overwritten by the next unit's first P.V
+                    if (h == G::kHalves - 1) {  // O_t may now be overwritten by the next unit's first P.V
                         tc_fence_before();
                         mbar_arrive(bar(BAR_OFREE + t));
                     }
@@ -811,7 +820,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // kernbench page's `_merge_running`, in log2 units:
 //   M = max_s m_s,  L = sum_s l_s 2^(m_s - M),  O = sum_s O_s 2^(m_s - M) / L,
 //   LSE = (M + log2 L) ln 2;  a row no piece saw a key of gets O = 0, LSE = -inf.
-// One warp per (split unit, tile, row); lane i owns columns 4i .. 4i+3.
+// One warp per (split unit, tile, row); lane i owns columns [i D/32, (i+1) D/32).
 struct CombineEntry {
     int unit;
     int first_slot;
@@ -827,7 +836,7 @@ struct CombineTable {
     CombineEntry e[kMaxCombine];
 };
 
-template <bool kF16>
+template <bool kF16, int kD>
 __global__ void __launch_bounds__(32 * kCombineWarps)
     splitkv_combine_kernel(const FwdParams p, const __grid_constant__ CombineTable ct) {
     const int gw = static_cast<int>(blockIdx.x) * kCombineWarps + static_cast<int>(threadIdx.x) / 32;
@@ -845,25 +854,37 @@ __global__ void __launch_bounds__(32 * kCombineWarps)
         const float2 ml = ct.ws_ml[((static_cast<size_t>(e.first_slot) + sl) * kTiles + t) * kBM + r];
         if (ml.y > 0.f) M = fmaxf(M, ml.x);
     }
+    constexpr int kPer = kD / 32;  // columns per lane (4 or 2)
     float L = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float acc[kPer] = {};
     for (int sl = 0; sl < e.n_slots; ++sl) {
         const size_t rr = ((static_cast<size_t>(e.first_slot) + sl) * kTiles + t) * kBM + r;
         const float2 ml = ct.ws_ml[rr];
         if (!(ml.y > 0.f)) continue;  // this piece saw no key of the row
         const float a = exp2f(ml.x - M);
-        const float4 v = reinterpret_cast<const float4*>(ct.ws_o + rr * kHeadDim)[lane];
+        const float* src = ct.ws_o + rr * kD + kPer * lane;
+        float v[kPer];
+        if constexpr (kPer == 4) {
+            const float4 x = *reinterpret_cast<const float4*>(src);
+            v[0] = x.x, v[1] = x.y, v[2] = x.z, v[3] = x.w;
+        } else {
+            const float2 x = *reinterpret_cast<const float2*>(src);
+            v[0] = x.x, v[1] = x.y;
+        }
         L += ml.y * a;
-        acc.x += v.x * a;
-        acc.y += v.y * a;
-        acc.z += v.z * a;
-        acc.w += v.w * a;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) acc[i] += v[i] * a;
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
-    uint2 out;
-    out.x = pack_x2<kF16>(acc.x * inv, acc.y * inv);
-    out.y = pack_x2<kF16>(acc.z * inv, acc.w * inv);
-    reinterpret_cast<uint2*>(ct.o + ((static_cast<size_t>(w.b) * p.Sq + row) * p.Hq + w.hq(t)) * kHeadDim)[lane] = out;
+    uint16_t* dst = ct.o + ((static_cast<size_t>(w.b) * p.Sq + row) * p.Hq + w.hq(t)) * kD + kPer * lane;
+    if constexpr (kPer == 4) {
+        uint2 out;
+        out.x = pack_x2<kF16>(acc[0] * inv, acc[1] * inv);
+        out.y = pack_x2<kF16>(acc[2] * inv, acc[3] * inv);
+        *reinterpret_cast<uint2*>(dst) = out;
+    } else {
+        *reinterpret_cast<uint32_t*>(dst) = pack_x2<kF16>(acc[0] * inv, acc[1] * inv);
+    }
     if (lane == 0 && p.lse != nullptr)
         p.lse[(static_cast<size_t>(w.b) * p.Hq + w.hq(t)) * p.Sq + row] =
             L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;

@@ -44,7 +44,7 @@ def test_bad_tensors_raise_without_launch():
     with pytest.raises(fa.AttnError):
         fa.attn_fwd(q, k[:, :, :1].contiguous(), k)      # k/v shape mismatch
     with pytest.raises(fa.AttnError) as e:
-        fa.attn_fwd(q[..., :64].contiguous(), k[..., :64].contiguous(), k[..., :64].contiguous())
+        fa.attn_fwd(q[..., :32].contiguous(), k[..., :32].contiguous(), k[..., :32].contiguous())
     assert e.value.status == fa.ATTN_ERR_UNSUPPORTED
     with pytest.raises(fa.AttnError) as e:
         flat = torch.zeros(64 * 2 * 128 + 8, dtype=torch.bfloat16, device="cuda")
