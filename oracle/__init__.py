@@ -12,6 +12,10 @@ Contents
   * ``partial_triple`` / ``merge_triples`` -- un-normalised (m, l, o) of a row
     over a key range, and the merge rule of the kernbench page
     (``_gqa_attention_prefill_short.py``, ``_merge_running``).
+  * ``attn_bwd`` / ``attn_bwd_dq_rows`` / ``attn_bwd_dkv_keys`` -- the C
+    oracle's gradients dq, dk, dv of sum(dO * o) in fp64: the plain
+    vector-Jacobian product of the definition (the Pallas page's
+    ``_attention_bwd``), for every element or for sampled rows / keys.
   * ``round_bf16`` -- exact round-to-nearest-even of fp64 values to bf16, the
     comparison value for the bf16 output.
   * ``twin`` (module ``oracle.twin``) -- an independent numpy fp64 restatement
@@ -61,6 +65,15 @@ def configure(lib):
     lib.oracle_partial_triple.argtypes = [P, P, P, L, L, L, L, L, L, ctypes.c_int,
                                           ctypes.c_double, ctypes.c_int, L, L, L, L, L, P, P, P]
     lib.oracle_partial_triple.restype = ctypes.c_int
+    lib.oracle_attn_bwd.argtypes = [P, P, P, P, L, L, L, L, L, L, ctypes.c_int,
+                                    ctypes.c_double, ctypes.c_int, P, P, P]
+    lib.oracle_attn_bwd.restype = ctypes.c_int
+    lib.oracle_attn_bwd_dq_rows.argtypes = [P, P, P, P, L, L, L, L, L, L, ctypes.c_int,
+                                            ctypes.c_double, ctypes.c_int, L, P, P]
+    lib.oracle_attn_bwd_dq_rows.restype = ctypes.c_int
+    lib.oracle_attn_bwd_dkv_keys.argtypes = [P, P, P, P, L, L, L, L, L, L, ctypes.c_int,
+                                             ctypes.c_double, ctypes.c_int, L, P, P, P]
+    lib.oracle_attn_bwd_dkv_keys.restype = ctypes.c_int
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = ctypes.c_int
     return lib
@@ -138,6 +151,56 @@ def partial_triple(q, k, v, causal: int, scale: float, b: int, h: int, i: int,
     if rc != 0:
         raise ValueError("oracle_partial_triple rejected its arguments")
     return float(m[0]), float(l[0]), o
+
+
+def _check_do(q, do):
+    if do.dtype != np.uint16 or do.shape != q.shape or not do.flags.c_contiguous:
+        raise ValueError("do must be a C-contiguous uint16 array shaped like q")
+
+
+def attn_bwd(q, k, v, do, causal: int, scale: float, f16: bool = False):
+    """fp64 (dq [B,Sq,Hq,D], dk [B,Skv,Hkv,D], dv [B,Skv,Hkv,D]): the gradient of
+    sum(do * o) with o the attention output; do has q's shape and 16-bit format."""
+    B, Sq, Skv, Hq, Hkv, D = _check_inputs(q, k, v)
+    _check_do(q, do)
+    dq = np.zeros((B, Sq, Hq, D), dtype=np.float64)
+    dk = np.zeros((B, Skv, Hkv, D), dtype=np.float64)
+    dv = np.zeros((B, Skv, Hkv, D), dtype=np.float64)
+    rc = _load().oracle_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(do), B, Sq, Skv, Hq, Hkv, D,
+                                 int(causal), float(scale), int(bool(f16)), _ptr(dq), _ptr(dk),
+                                 _ptr(dv))
+    if rc != 0:
+        raise ValueError("oracle_attn_bwd rejected its arguments")
+    return dq, dk, dv
+
+
+def attn_bwd_dq_rows(q, k, v, do, rows, causal: int, scale: float, f16: bool = False):
+    """fp64 dq (len(rows) x D) of the listed (b, h, i) rows."""
+    B, Sq, Skv, Hq, Hkv, D = _check_inputs(q, k, v)
+    _check_do(q, do)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
+    dq = np.zeros((rows.shape[0], D), dtype=np.float64)
+    rc = _load().oracle_attn_bwd_dq_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(do), B, Sq, Skv, Hq,
+                                         Hkv, D, int(causal), float(scale), int(bool(f16)),
+                                         rows.shape[0], _ptr(rows), _ptr(dq))
+    if rc != 0:
+        raise ValueError("oracle_attn_bwd_dq_rows rejected its arguments")
+    return dq
+
+
+def attn_bwd_dkv_keys(q, k, v, do, keys, causal: int, scale: float, f16: bool = False):
+    """fp64 (dk, dv), each len(keys) x D, of the listed (b, g, j) keys (g: key/value head)."""
+    B, Sq, Skv, Hq, Hkv, D = _check_inputs(q, k, v)
+    _check_do(q, do)
+    keys = np.ascontiguousarray(np.asarray(keys, dtype=np.int64).reshape(-1, 3))
+    dk = np.zeros((keys.shape[0], D), dtype=np.float64)
+    dv = np.zeros((keys.shape[0], D), dtype=np.float64)
+    rc = _load().oracle_attn_bwd_dkv_keys(_ptr(q), _ptr(k), _ptr(v), _ptr(do), B, Sq, Skv, Hq,
+                                          Hkv, D, int(causal), float(scale), int(bool(f16)),
+                                          keys.shape[0], _ptr(keys), _ptr(dk), _ptr(dv))
+    if rc != 0:
+        raise ValueError("oracle_attn_bwd_dkv_keys rejected its arguments")
+    return dk, dv
 
 
 def merge_triples(t1, t2):

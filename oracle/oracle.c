@@ -33,6 +33,23 @@
  * The partial-triple entry point returns the un-normalised (m, l, o) of a row
  * over a sub-range of keys; merging such triples is the rule of the kernbench
  * page (`_merge_running`), used by the tests to pin the one-shot definition.
+ *
+ * Backward (gradients; the Pallas page's `_attention_bwd`, written out as the
+ * plain vector-Jacobian product of the definition above).  Given dO, the
+ * gradient of L = sum dO[b,i,h,d] * o[b,i,h,d] with respect to q, k and v:
+ *   p_ij    = exp(s_ij - lse_i)                 normalised weight, visible j only
+ *   dp_ij   = sum_d dO[b,i,h,d] * v[b,j,g,d]
+ *   delta_i = sum_j p_ij * dp_ij                (equals dO_i . o_i)
+ *   ds_ij   = p_ij * (dp_ij - delta_i)          (Jacobian of the row softmax)
+ *   dq[b,i,h,:] = scale * sum_j ds_ij * k[b,j,g,:]
+ *   dk[b,j,g,:] = scale * sum_{h in group g} sum_i ds_ij * q[b,i,h,:]
+ *   dv[b,j,g,:] =         sum_{h in group g} sum_i p_ij  * dO[b,i,h,:]
+ * The page sums per-query-head dk/dv over each group of heads sharing a
+ * key/value head; here the sums run over the group directly.  dO has q's
+ * layout and element format.  Rows with no visible key contribute nothing.
+ * The page's backward rejects the causal mask; these functions apply the same
+ * visibility rule as the forward (a masked pair has p_ij = 0), the gradient of
+ * the masked forward.
  */
 #include <math.h>
 #include <stdint.h>
@@ -232,6 +249,273 @@ int oracle_partial_triple(const uint16_t *q, const uint16_t *k, const uint16_t *
     free(s_buf);
     free(qd);
     return rc;
+}
+
+/* ------------------------------------------------------------------ backward */
+
+/* Weights and softmax-Jacobian terms of one row: on return p_buf[j] = p_ij and
+ * ds_buf[j] = ds_ij for j < *end_out (the row's visible keys), and, if dq is not
+ * NULL, dq[0..D) = scale * sum_j ds_ij k_j.  qd, dod: D doubles of scratch.
+ * Three passes over the keys: logits and their max; weights, lse and dp_ij with
+ * delta_i; ds_ij and dq. */
+static void row_grad(const problem_t *p, const uint16_t *dO, long b, long h, long i,
+                     double *p_buf, double *ds_buf, double *qd, double *dod, double *dq,
+                     long *end_out) {
+    const long D = p->D;
+    const long g = h / (p->Hq / p->Hkv);
+    const long end = visible_end(p, i);
+    *end_out = end > 0 ? end : 0;
+    if (dq)
+        for (long d = 0; d < D; ++d) dq[d] = 0.0;
+    if (end <= 0) return;
+    const long qoff = ((b * p->Sq + i) * p->Hq + h) * D;
+    for (long d = 0; d < D; ++d) {
+        qd[d] = widen(p, p->q[qoff + d]);
+        dod[d] = widen(p, dO[qoff + d]);
+    }
+    /* pass 1: scaled logits (kept in p_buf) and their maximum */
+    double m = -INFINITY;
+    for (long j = 0; j < end; ++j) {
+        const uint16_t *krow = p->k + ((b * p->Skv + j) * p->Hkv + g) * D;
+        double acc = 0.0;
+        for (long d = 0; d < D; ++d) acc += qd[d] * widen(p, krow[d]);
+        p_buf[j] = p->scale * acc;
+        if (p_buf[j] > m) m = p_buf[j];
+    }
+    double l = 0.0;
+    for (long j = 0; j < end; ++j) l += exp(p_buf[j] - m);
+    const double lse = m + log(l);
+    /* pass 2: normalised weights, dp_ij (kept in ds_buf) and delta_i */
+    double delta = 0.0;
+    for (long j = 0; j < end; ++j) {
+        p_buf[j] = exp(p_buf[j] - lse);
+        const uint16_t *vrow = p->v + ((b * p->Skv + j) * p->Hkv + g) * D;
+        double dp = 0.0;
+        for (long d = 0; d < D; ++d) dp += dod[d] * widen(p, vrow[d]);
+        ds_buf[j] = dp;
+        delta += p_buf[j] * dp;
+    }
+    /* pass 3: ds_ij and dq */
+    for (long j = 0; j < end; ++j) {
+        ds_buf[j] = p_buf[j] * (ds_buf[j] - delta);
+        if (dq) {
+            const uint16_t *krow = p->k + ((b * p->Skv + j) * p->Hkv + g) * D;
+            for (long d = 0; d < D; ++d) dq[d] += ds_buf[j] * widen(p, krow[d]);
+        }
+    }
+    if (dq)
+        for (long d = 0; d < D; ++d) dq[d] *= p->scale;
+}
+
+/*
+ * Every gradient.  dO: [B,Sq,Hq,D] 16-bit patterns in q's format.
+ * dq_out: [B,Sq,Hq,D] doubles; dk_out, dv_out: [B,Skv,Hkv,D] doubles.
+ * Parallel over (b, g): each thread owns the dk/dv rows of its key/value head.
+ */
+int oracle_attn_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *dO,
+                    long B, long Sq, long Skv, long Hq, long Hkv, long D, int causal,
+                    double scale, int f16, double *dq_out, double *dk_out, double *dv_out) {
+    if (check_dims(B, Sq, Skv, Hq, Hkv, D) || causal < 0 || causal > 2) return -1;
+    problem_t p = {q, k, v, B, Sq, Skv, Hq, Hkv, D, causal, scale, f16 != 0};
+    const long G = Hq / Hkv;
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *p_buf = (double *)malloc(sizeof(double) * (size_t)Skv);
+        double *ds_buf = (double *)malloc(sizeof(double) * (size_t)Skv);
+        double *qd = (double *)malloc(sizeof(double) * (size_t)D);
+        double *dod = (double *)malloc(sizeof(double) * (size_t)D);
+        if (!p_buf || !ds_buf || !qd || !dod) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (long bg = 0; bg < B * Hkv; ++bg) {
+                const long b = bg / Hkv, g = bg % Hkv;
+                for (long j = 0; j < Skv; ++j)
+                    for (long d = 0; d < D; ++d) {
+                        dk_out[((b * Skv + j) * Hkv + g) * D + d] = 0.0;
+                        dv_out[((b * Skv + j) * Hkv + g) * D + d] = 0.0;
+                    }
+                for (long h = g * G; h < (g + 1) * G; ++h)
+                    for (long i = 0; i < Sq; ++i) {
+                        long end;
+                        double *dq = dq_out + ((b * Sq + i) * Hq + h) * D;
+                        row_grad(&p, dO, b, h, i, p_buf, ds_buf, qd, dod, dq, &end);
+                        for (long j = 0; j < end; ++j) {
+                            double *dk = dk_out + ((b * Skv + j) * Hkv + g) * D;
+                            double *dv = dv_out + ((b * Skv + j) * Hkv + g) * D;
+                            for (long d = 0; d < D; ++d) {
+                                dk[d] += scale * ds_buf[j] * qd[d];
+                                dv[d] += p_buf[j] * dod[d];
+                            }
+                        }
+                    }
+            }
+        }
+        free(p_buf);
+        free(ds_buf);
+        free(qd);
+        free(dod);
+    }
+    return bad ? -1 : 0;
+}
+
+/*
+ * dq of an explicit list of rows: rows holds nrows triples (b, h, i);
+ * dq_out: nrows*D doubles.
+ */
+int oracle_attn_bwd_dq_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                            const uint16_t *dO, long B, long Sq, long Skv, long Hq, long Hkv,
+                            long D, int causal, double scale, int f16, long nrows,
+                            const long *rows, double *dq_out) {
+    if (check_dims(B, Sq, Skv, Hq, Hkv, D) || causal < 0 || causal > 2) return -1;
+    problem_t p = {q, k, v, B, Sq, Skv, Hq, Hkv, D, causal, scale, f16 != 0};
+    for (long r = 0; r < nrows; ++r) {
+        const long *t = rows + 3 * r;
+        if (t[0] < 0 || t[0] >= B || t[1] < 0 || t[1] >= Hq || t[2] < 0 || t[2] >= Sq)
+            return -1;
+    }
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *p_buf = (double *)malloc(sizeof(double) * (size_t)Skv);
+        double *ds_buf = (double *)malloc(sizeof(double) * (size_t)Skv);
+        double *qd = (double *)malloc(sizeof(double) * (size_t)D);
+        double *dod = (double *)malloc(sizeof(double) * (size_t)D);
+        if (!p_buf || !ds_buf || !qd || !dod) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (long r = 0; r < nrows; ++r) {
+                const long *t = rows + 3 * r;
+                long end;
+                row_grad(&p, dO, t[0], t[1], t[2], p_buf, ds_buf, qd, dod, dq_out + r * D,
+                         &end);
+            }
+        }
+        free(p_buf);
+        free(ds_buf);
+        free(qd);
+        free(dod);
+    }
+    return bad ? -1 : 0;
+}
+
+/*
+ * dk and dv of an explicit list of keys: keys holds nkeys triples (b, g, j)
+ * with g a key/value head; dk_out, dv_out: nkeys*D doubles each.  For every
+ * (b, g) that occurs, the per-row lse_i and delta_i of the group's query heads
+ * are computed once (one row pass each), then each listed key sums over the
+ * rows that see it.
+ */
+int oracle_attn_bwd_dkv_keys(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                             const uint16_t *dO, long B, long Sq, long Skv, long Hq, long Hkv,
+                             long D, int causal, double scale, int f16, long nkeys,
+                             const long *keys, double *dk_out, double *dv_out) {
+    if (check_dims(B, Sq, Skv, Hq, Hkv, D) || causal < 0 || causal > 2) return -1;
+    problem_t p = {q, k, v, B, Sq, Skv, Hq, Hkv, D, causal, scale, f16 != 0};
+    for (long r = 0; r < nkeys; ++r) {
+        const long *t = keys + 3 * r;
+        if (t[0] < 0 || t[0] >= B || t[1] < 0 || t[1] >= Hkv || t[2] < 0 || t[2] >= Skv)
+            return -1;
+    }
+    const long G = Hq / Hkv;
+    double *lse = (double *)malloc(sizeof(double) * (size_t)(G * Sq));
+    double *delta = (double *)malloc(sizeof(double) * (size_t)(G * Sq));
+    char *done = (char *)calloc((size_t)(B * Hkv), 1);
+    int bad = (!lse || !delta || !done);
+    for (long r0 = 0; r0 < nkeys && !bad; ++r0) {
+        const long b = keys[3 * r0], g = keys[3 * r0 + 1];
+        if (done[b * Hkv + g]) continue;
+        done[b * Hkv + g] = 1;
+        /* lse_i and delta_i of every row of the group's heads */
+#pragma omp parallel
+        {
+            double *p_buf = (double *)malloc(sizeof(double) * (size_t)Skv);
+            double *ds_buf = (double *)malloc(sizeof(double) * (size_t)Skv);
+            double *qd = (double *)malloc(sizeof(double) * (size_t)D);
+            double *dod = (double *)malloc(sizeof(double) * (size_t)D);
+            if (!p_buf || !ds_buf || !qd || !dod) {
+#pragma omp atomic write
+                bad = 1;
+            } else {
+#pragma omp for schedule(dynamic, 4)
+                for (long hi = 0; hi < G * Sq; ++hi) {
+                    const long h = g * G + hi / Sq, i = hi % Sq;
+                    const long end = visible_end(&p, i);
+                    if (end <= 0) {
+                        lse[hi] = -INFINITY;
+                        delta[hi] = 0.0;
+                        continue;
+                    }
+                    const long qoff = ((b * Sq + i) * Hq + h) * D;
+                    for (long d = 0; d < D; ++d) {
+                        qd[d] = widen(&p, q[qoff + d]);
+                        dod[d] = widen(&p, dO[qoff + d]);
+                    }
+                    double m = -INFINITY;
+                    for (long j = 0; j < end; ++j) {
+                        const uint16_t *krow = k + ((b * Skv + j) * Hkv + g) * D;
+                        double acc = 0.0;
+                        for (long d = 0; d < D; ++d) acc += qd[d] * widen(&p, krow[d]);
+                        p_buf[j] = scale * acc;
+                        if (p_buf[j] > m) m = p_buf[j];
+                    }
+                    double l = 0.0;
+                    for (long j = 0; j < end; ++j) l += exp(p_buf[j] - m);
+                    const double ls = m + log(l);
+                    double dl = 0.0;
+                    for (long j = 0; j < end; ++j) {
+                        const uint16_t *vrow = v + ((b * Skv + j) * Hkv + g) * D;
+                        double dp = 0.0;
+                        for (long d = 0; d < D; ++d) dp += dod[d] * widen(&p, vrow[d]);
+                        dl += exp(p_buf[j] - ls) * dp;
+                    }
+                    lse[hi] = ls;
+                    delta[hi] = dl;
+                }
+            }
+            free(p_buf);
+            free(ds_buf);
+            free(qd);
+            free(dod);
+        }
+        if (bad) break;
+        /* every listed key of this (b, g) */
+#pragma omp parallel for schedule(dynamic, 1)
+        for (long r = 0; r < nkeys; ++r) {
+            if (keys[3 * r] != b || keys[3 * r + 1] != g) continue;
+            const long j = keys[3 * r + 2];
+            double *dk = dk_out + r * D;
+            double *dv = dv_out + r * D;
+            for (long d = 0; d < D; ++d) dk[d] = dv[d] = 0.0;
+            const uint16_t *krow = k + ((b * Skv + j) * Hkv + g) * D;
+            const uint16_t *vrow = v + ((b * Skv + j) * Hkv + g) * D;
+            for (long hi = 0; hi < G * Sq; ++hi) {
+                const long h = g * G + hi / Sq, i = hi % Sq;
+                if (j >= visible_end(&p, i)) continue;
+                const uint16_t *qrow = q + ((b * Sq + i) * Hq + h) * D;
+                const uint16_t *dorow = dO + ((b * Sq + i) * Hq + h) * D;
+                double s = 0.0, dp = 0.0;
+                for (long d = 0; d < D; ++d) {
+                    s += widen(&p, qrow[d]) * widen(&p, krow[d]);
+                    dp += widen(&p, dorow[d]) * widen(&p, vrow[d]);
+                }
+                const double pij = exp(scale * s - lse[hi]);
+                const double ds = pij * (dp - delta[hi]);
+                for (long d = 0; d < D; ++d) {
+                    dk[d] += scale * ds * widen(&p, qrow[d]);
+                    dv[d] += pij * widen(&p, dorow[d]);
+                }
+            }
+        }
+    }
+    free(lse);
+    free(delta);
+    free(done);
+    return bad ? -1 : 0;
 }
 
 /* Number of OpenMP threads the oracle runs with (1 without OpenMP). */

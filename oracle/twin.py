@@ -22,7 +22,13 @@ def _widen(bits, f16=False):
 
 def attention(q_bits, k_bits, v_bits, causal: int, scale: float, f16: bool = False):
     """Returns (o [B,Sq,Hq,D] fp64, lse [B,Hq,Sq] fp64); f16: binary16 inputs."""
-    q, k, v = _widen(q_bits, f16), _widen(k_bits, f16), _widen(v_bits, f16)
+    return attention_values(_widen(q_bits, f16), _widen(k_bits, f16), _widen(v_bits, f16),
+                            causal, scale)
+
+
+def attention_values(q, k, v, causal: int, scale: float):
+    """The same on fp64 arrays (any real values, e.g. perturbed inputs)."""
+    q, k, v = (np.asarray(t, dtype=np.float64) for t in (q, k, v))
     B, Sq, Hq, D = q.shape
     Skv, Hkv = k.shape[1], k.shape[2]
     group = Hq // Hkv

@@ -39,6 +39,27 @@ MUTANTS = [
      "mag = ldexp((double)(1024 + frac), e - 24);"),
     ("f16_subnormal_scale", "mag = ldexp((double)frac, -24); /* zero and subnormals */",
      "mag = ldexp((double)frac, -25);"),
+    # backward
+    ("bwd_dq_no_scale", "dq[d] *= p->scale;", ";"),
+    ("bwd_delta_sign", "ds_buf[j] = p_buf[j] * (ds_buf[j] - delta);",
+     "ds_buf[j] = p_buf[j] * (ds_buf[j] + delta);"),
+    ("bwd_no_delta", "ds_buf[j] = p_buf[j] * (ds_buf[j] - delta);",
+     "ds_buf[j] = p_buf[j] * ds_buf[j];"),
+    ("bwd_unnormalised_weights", "p_buf[j] = exp(p_buf[j] - lse);", "p_buf[j] = exp(p_buf[j] - m);"),
+    ("bwd_dv_from_ds", "dv[d] += p_buf[j] * dod[d];", "dv[d] += ds_buf[j] * dod[d];"),
+    ("bwd_dk_from_do", "dk[d] += scale * ds_buf[j] * qd[d];", "dk[d] += scale * ds_buf[j] * dod[d];"),
+    ("bwd_dk_no_scale", "dk[d] += scale * ds_buf[j] * qd[d];", "dk[d] += ds_buf[j] * qd[d];"),
+    ("bwd_dp_from_q", "dp += dod[d] * widen(p, vrow[d]);", "dp += qd[d] * widen(p, vrow[d]);"),
+    ("bwd_dq_from_p", "dq[d] += ds_buf[j] * widen(p, krow[d]);",
+     "dq[d] += p_buf[j] * widen(p, krow[d]);"),
+    ("bwd_strided_group", "for (long h = g * G; h < (g + 1) * G; ++h)",
+     "for (long h = g; h < Hq; h += Hkv)"),
+    ("bwd_keys_base2", "const double pij = exp(scale * s - lse[hi]);",
+     "const double pij = exp2(scale * s - lse[hi]);"),
+    ("bwd_keys_delta_sign", "const double ds = pij * (dp - delta[hi]);",
+     "const double ds = pij * (dp + delta[hi]);"),
+    ("bwd_keys_mask_off_by_one", "if (j >= visible_end(&p, i)) continue;",
+     "if (j > visible_end(&p, i)) continue;"),
 ]
 
 PIN_TESTS = [
@@ -48,6 +69,14 @@ PIN_TESTS = [
     "test_bottom_right_equals_tail_of_square_causal", "test_shift_invariance_large_logits",
     "test_merge_identity_random_chunks", "test_top_left_rules",
     "test_f16_widening_every_finite_pattern", "test_f16_brute_force_twin",
+]
+
+BWD_PIN_TESTS = [
+    "test_bwd_finite_differences", "test_bwd_matches_torch_autograd",
+    "test_bwd_hand_worked_two_keys", "test_bwd_zero_query_closed_form",
+    "test_bwd_constant_values_give_zero_dq_dk", "test_bwd_invariants",
+    "test_bwd_gqa_equals_repeated_heads", "test_bwd_sampled_entry_points_match_full",
+    "test_bwd_fully_masked_rows_contribute_nothing",
 ]
 
 
@@ -63,11 +92,12 @@ def _build_mutant(tmp_path, name, old, new):
 
 
 def _run_pins(monkeypatch, lib):
+    import test_oracle_bwd_pins as bwd_pins
     import test_oracle_pins as pins
     monkeypatch.setattr(oracle, "_lib", lib)
     failures = 0
-    for name in PIN_TESTS:
-        fn = getattr(pins, name)
+    for module, name in [(pins, n) for n in PIN_TESTS] + [(bwd_pins, n) for n in BWD_PIN_TESTS]:
+        fn = getattr(module, name)
         params = getattr(fn, "pytestmark", [])
         cases = [dict()]
         for mark in params:
