@@ -1,6 +1,7 @@
-"""GB300-native fused attention forward (sm_103a), exported through libattn's C ABI.
+"""GB300-native fused attention (sm_103a): forward and backward, exported through
+libattn's C ABI.
 
-The Python layer only marshals arguments: every step of the forward pass runs
+The Python layer only marshals arguments: every step of both passes runs
 in the CUDA kernels of ``libattn.so``.  Importing this package does not load
 the library; the first call does, and it raises if the library is missing.
 """
@@ -10,5 +11,5 @@ from ._binding import (  # noqa: F401
     attn_fwd_splitkv_workspace_size, attn_fwd_splitkv_noalloc_ptr, attn_status_str,
     attn_check_device_status,
     attn_kernel_launches, attn_debug_wait_timeout, library_path, load_library,
-    exported_symbols,
+    exported_symbols, attn_bwd, attn_bwd_ptr, attn_bwd_workspace_size,
 )

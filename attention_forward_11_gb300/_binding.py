@@ -24,7 +24,7 @@ _LIB_NAME = "libattn.so"
 # Every symbol include/attn.h declares (checked by the CPU tests).
 EXPORTED = ("attn_fwd", "attn_fwd_ex", "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_size",
             "attn_fwd_splitkv_noalloc", "attn_status_str", "attn_check_device_status",
-            "attn_kernel_launches", "attn_debug_wait_timeout")
+            "attn_kernel_launches", "attn_debug_wait_timeout", "attn_bwd", "attn_bwd_workspace_size")
 
 _lock = threading.Lock()
 _lib = None
@@ -78,6 +78,11 @@ def load_library():
         lib.attn_fwd_splitkv_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I,
                                                  ctypes.c_float, P]
         lib.attn_fwd_splitkv_noalloc.restype = I
+        lib.attn_bwd_workspace_size.argtypes = [I, I, I, I, I, I, ctypes.POINTER(ctypes.c_size_t)]
+        lib.attn_bwd_workspace_size.restype = I
+        lib.attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, ctypes.c_float, I, P,
+                                 ctypes.c_size_t, P]
+        lib.attn_bwd.restype = I
         _lib = lib
         return lib
 
@@ -210,6 +215,56 @@ def attn_fwd_splitkv_noalloc_ptr(q: int, k: int, v: int, o: int, lse: int, B: in
     inside libattn.  Returns the attn_status_t value."""
     return int(load_library().attn_fwd_splitkv_noalloc(q, k, v, o, lse, B, Sq, Skv, Hq, Hkv, D,
                                                        causal, ctypes.c_float(scale), stream))
+
+
+def attn_bwd_workspace_size(B: int, Sq: int, Skv: int, Hq: int, Hkv: int, D: int) -> int:
+    n = ctypes.c_size_t(0)
+    st = load_library().attn_bwd_workspace_size(B, Sq, Skv, Hq, Hkv, D, ctypes.byref(n))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_bwd_workspace_size")
+    return int(n.value)
+
+
+def attn_bwd_ptr(q: int, k: int, v: int, o: int, lse: int, do: int, dq: int, dk: int, dv: int,
+                 B: int, Sq: int, Skv: int, Hq: int, Hkv: int, D: int, causal: int, scale: float,
+                 dtype: int, workspace: int, workspace_bytes: int, stream: int) -> int:
+    """Raw C-ABI call (device pointers as ints); returns the status code."""
+    return load_library().attn_bwd(q, k, v, o, lse, do, dq, dk, dv, B, Sq, Skv, Hq, Hkv, D,
+                                   int(causal), float(scale), int(dtype), workspace,
+                                   int(workspace_bytes), stream)
+
+
+def attn_bwd(q, k, v, o, lse, do, causal: int = 0, scale: float | None = None, dq=None, dk=None,
+             dv=None, workspace=None, stream=None):
+    """dq, dk, dv of sum(do * o) for o = attn_fwd(q, k, v, causal, scale); o and lse
+    are that forward's outputs.  bf16 or float16 CUDA tensors (all the same type),
+    lse fp32 [B, Hq, Sq].  Outputs and the workspace are allocated here if None."""
+    import torch
+    B, Sq, Hq, D = q.shape
+    Skv, Hkv = k.shape[1], k.shape[2]
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise AttnError(ATTN_ERR_INVALID_ARG, "q must be bf16 or float16")
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
+        if t.dtype != q.dtype or not t.is_cuda or not t.is_contiguous():
+            raise AttnError(ATTN_ERR_INVALID_ARG, f"{name} must be a contiguous CUDA tensor of q's dtype")
+    if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous():
+        raise AttnError(ATTN_ERR_INVALID_ARG, "lse must be a contiguous fp32 CUDA tensor")
+    dtype = ATTN_DTYPE_F16 if q.dtype == torch.float16 else ATTN_DTYPE_BF16
+    if scale is None:
+        scale = 1.0 / (D ** 0.5)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        workspace = torch.empty(attn_bwd_workspace_size(B, Sq, Skv, Hq, Hkv, D), dtype=torch.uint8,
+                                device=q.device)
+    st = attn_bwd_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                      do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Sq, Skv, Hq,
+                      Hkv, D, int(causal), float(scale), dtype, workspace.data_ptr(),
+                      workspace.numel(), _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_bwd")
+    return dq, dk, dv
 
 
 def attn_check_device_status(stream=None) -> int:

@@ -17,6 +17,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "fmha_bwd_sm103.cuh"
 #include "fmha_fwd_sm103.cuh"
 
 namespace {
@@ -67,6 +68,15 @@ bool opt_in_smem() {
                                 attn::Geo<kD>::kSmemBytes) == cudaSuccess;
 }
 
+template <bool kF16, int kD>
+bool opt_in_smem_bwd() {
+    constexpr int bytes = attn::bwd::BwdGeo<kD>::kSmemBytes;
+    return cudaFuncSetAttribute(attn::bwd::fmha_bwd_dkdv_kernel<kF16, kD>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess &&
+           cudaFuncSetAttribute(attn::bwd::fmha_bwd_dq_kernel<kF16, kD>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess;
+}
+
 // Per-device one-time set-up: the kernels' shared-memory opt-in and the SM count.
 bool device_setup(int dev, int* sm_count) {
     static std::mutex mu;
@@ -78,6 +88,8 @@ bool device_setup(int dev, int* sm_count) {
         if (!opt_in_smem<attn::PlainSched, false, 128>() || !opt_in_smem<attn::PlainSched, true, 128>() ||
             !opt_in_smem<attn::SplitSched, false, 128>() || !opt_in_smem<attn::PlainSched, false, 64>() ||
             !opt_in_smem<attn::PlainSched, true, 64>() || !opt_in_smem<attn::SplitSched, false, 64>() ||
+            !opt_in_smem_bwd<false, 128>() || !opt_in_smem_bwd<true, 128>() || !opt_in_smem_bwd<false, 64>() ||
+            !opt_in_smem_bwd<true, 64>() ||
             cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
             return false;
         sms[dev] = n;
@@ -486,6 +498,115 @@ extern "C" attn_status_t attn_fwd_splitkv_noalloc(const void* q, const void* k, 
     CUtensorMap tm[4];
     if (!encode_maps(q, k, v, o, B, Sq, Skv, Hq, Hkv, D, tm)) return ATTN_ERR_CUDA;
     return plan.split ? launch_split(tm, p, plan, scratch, stream) : launch_plain(tm, p, sms, stream);
+}
+
+// ---- backward
+namespace {
+
+constexpr size_t kBwdAlign = 256;
+
+size_t bwd_vec_bytes(int B, int Sq, int Hq) {
+    const size_t sq_pad = (static_cast<size_t>(Sq) + attn::kBM - 1) / attn::kBM * attn::kBM;
+    const size_t v = static_cast<size_t>(B) * Hq * sq_pad * sizeof(float);
+    return (v + kBwdAlign - 1) / kBwdAlign * kBwdAlign;
+}
+
+template <bool kF16, int kD>
+attn_status_t launch_bwd(const CUtensorMap* tm, const void* o, const void* dO, const float* lse,
+                         const attn::bwd::BwdParams& p, cudaStream_t stream) {
+    using namespace attn::bwd;
+    const long long rows = (long long)p.B * p.Hq * p.sq_pad;
+    bwd_prep_kernel<kF16, kD><<<static_cast<unsigned int>((rows + 7) / 8), 256, 0, stream>>>(
+        static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dO), lse, p);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    const unsigned int g_kv = static_cast<unsigned int>(p.B * p.Hkv * p.n_kv_tiles);
+    fmha_bwd_dkdv_kernel<kF16, kD><<<g_kv, kThreads, BwdGeo<kD>::kSmemBytes, stream>>>(tm[0], tm[1], tm[2], tm[3], p);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    const unsigned int g_q = static_cast<unsigned int>(p.B * p.Hq * p.n_q_tiles);
+    fmha_bwd_dq_kernel<kF16, kD><<<g_q, kThreads, BwdGeo<kD>::kSmemBytes, stream>>>(tm[0], tm[1], tm[2], tm[3], p);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" attn_status_t attn_bwd_workspace_size(int B, int Sq, int Skv, int Hq, int Hkv, int D, size_t* bytes) {
+    if (!bytes) return ATTN_ERR_INVALID_ARG;
+    *bytes = 0;
+    const attn_status_t st = check_sizes(B, Sq, Skv, Hq, Hkv, D, 0);
+    if (st != ATTN_OK) return st;
+    *bytes = 2 * bwd_vec_bytes(B, Sq, Hq);
+    return ATTN_OK;
+}
+
+extern "C" attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                                  const void* dO, void* dq, void* dk, void* dv, int B, int Sq, int Skv, int Hq,
+                                  int Hkv, int D, int causal, float scale, int dtype, void* workspace,
+                                  size_t workspace_bytes, cudaStream_t stream) {
+    // ---- validation: nothing is launched on any error
+    if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !workspace) return ATTN_ERR_INVALID_ARG;
+    if (dtype != ATTN_DTYPE_BF16 && dtype != ATTN_DTYPE_F16) return ATTN_ERR_INVALID_ARG;
+    const attn_status_t st = check_sizes(B, Sq, Skv, Hq, Hkv, D, causal);
+    if (st == ATTN_ERR_INVALID_ARG) return st;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+    for (const void* ptr : {q, k, v, o, dO, static_cast<const void*>(dq), static_cast<const void*>(dk),
+                            static_cast<const void*>(dv)})
+        if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return ATTN_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(lse) % 4 != 0 || reinterpret_cast<uintptr_t>(workspace) % kBwdAlign != 0)
+        return ATTN_ERR_INVALID_ARG;
+    const int Dn = D > 0 ? D : 1;
+    const size_t q_bytes = (size_t)B * Sq * Hq * Dn * 2, kv_bytes = (size_t)B * Skv * Hkv * Dn * 2;
+    const size_t lse_bytes = (size_t)B * Hq * Sq * 4;
+    const size_t need = 2 * bwd_vec_bytes(B, Sq, Hq);
+    if (workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
+    // the outputs and the workspace overlap no input and no other output
+    const void* out_p[4] = {dq, dk, dv, workspace};
+    const size_t out_n[4] = {q_bytes, kv_bytes, kv_bytes, need};
+    const void* in_p[6] = {q, k, v, o, lse, dO};
+    const size_t in_n[6] = {q_bytes, kv_bytes, kv_bytes, q_bytes, lse_bytes, q_bytes};
+    for (int a = 0; a < 4; ++a) {
+        for (int c = 0; c < 6; ++c)
+            if (ranges_overlap(out_p[a], out_n[a], in_p[c], in_n[c])) return ATTN_ERR_INVALID_ARG;
+        for (int c = a + 1; c < 4; ++c)
+            if (ranges_overlap(out_p[a], out_n[a], out_p[c], out_n[c])) return ATTN_ERR_INVALID_ARG;
+    }
+    if (st != ATTN_OK) return st;  // valid request, unsupported head size
+    attn::bwd::BwdParams p{};
+    p.B = B;
+    p.Sq = Sq;
+    p.Skv = Skv;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.D = D;
+    p.causal = causal;
+    p.diag = causal == 1 ? Skv - Sq : 0;
+    p.n_q_tiles = (Sq + attn::kBM - 1) / attn::kBM;
+    p.n_kv_tiles = (Skv + attn::kBN - 1) / attn::kBN;
+    p.sq_pad = p.n_q_tiles * attn::kBM;
+    if ((long long)B * Hkv * p.n_kv_tiles > 0x7fffffffLL || (long long)B * Hq * p.n_q_tiles > 0x7fffffffLL ||
+        ((long long)B * Hq * p.sq_pad + 7) / 8 > 0x7fffffffLL)
+        return ATTN_ERR_INVALID_ARG;
+    p.scale = scale;
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    p.lse2 = static_cast<float*>(workspace);
+    p.delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + bwd_vec_bytes(B, Sq, Hq));
+    p.dq = static_cast<uint16_t*>(dq);
+    p.dk = static_cast<uint16_t*>(dk);
+    p.dv = static_cast<uint16_t*>(dv);
+    p.poll_limit = kDefaultPollLimit;
+    const bool f16 = dtype == ATTN_DTYPE_F16;
+    CUtensorMap tm[4];
+    if (!encode_bshd(&tm[0], q, B, Sq, Hq, D, f16) || !encode_bshd(&tm[1], dO, B, Sq, Hq, D, f16) ||
+        !encode_bshd(&tm[2], k, B, Skv, Hkv, D, f16) || !encode_bshd(&tm[3], v, B, Skv, Hkv, D, f16))
+        return ATTN_ERR_CUDA;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || !device_setup(dev, &sms)) return ATTN_ERR_CUDA;
+    if (D == 64)
+        return f16 ? launch_bwd<true, 64>(tm, o, dO, lse, p, stream) : launch_bwd<false, 64>(tm, o, dO, lse, p, stream);
+    return f16 ? launch_bwd<true, 128>(tm, o, dO, lse, p, stream) : launch_bwd<false, 128>(tm, o, dO, lse, p, stream);
 }
 
 extern "C" const char* attn_status_str(attn_status_t status) {

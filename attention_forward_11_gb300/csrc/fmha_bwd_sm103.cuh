@@ -1,0 +1,726 @@
+// fmha_bwd_sm103.cuh -- attention backward for sm_103a (GB300).
+//
+// Given Q, K, V, the forward output O, its LSE and the output gradient dO, the
+// three kernels below produce dQ, dK and dV: the Pallas page's
+// `_attention_bwd` (delta = rowsum(O * dO); a dQ kernel that walks the KV
+// tiles of one query tile; a dK/dV kernel that walks the query tiles of one KV
+// tile), rebuilt on tcgen05 with tensor-memory accumulators.
+//
+//   prep    delta_i = sum_d dO[i,d] O[i,d] and lse2_i = lse_i * log2(e) of every
+//           query row into a padded workspace (+inf / 0 on padding and on rows
+//           that see no key, so their weights vanish without a mask).
+//   dK/dV   one CTA per (batch, key/value head, 128-key tile).  For every query
+//           head of the group and every 128-row query tile that sees a key of
+//           the tile:
+//             S^T  = K Q^T            (tensor memory, 128 keys x 128 rows)
+//             dP^T = V dO^T
+//             P^T  = 2^(S^T scale log2e - lse2)       (bf16, over S^T)
+//             dS^T = P^T (dP^T - delta)               (bf16, over dP^T)
+//             dV  += P^T dO,   dK += dS^T Q           (A operands from tensor memory)
+//           The group's query heads accumulate into the same dK/dV, which is
+//           the page's sum of per-head dK/dV over each group, done in place.
+//   dQ      one CTA per (batch, query head, 128-row tile), over its visible KV tiles:
+//             S = Q K^T,  dP = dO V^T,  dS = P (dP - delta)   (bf16, over dP)
+//             dQ += dS K
+//   dQ and dK carry the softmax scale (applied to the fp32 accumulators).
+//
+// Warp roles (320 threads): warps 0-7 elementwise work (warp w owns TMEM lane
+// quarter w % 4 and one half of the 128 columns: w / 4), warp 8 issues the MMAs
+// (one elected lane), warp 9 drives the TMA copies.  The operand that stays
+// fixed for the CTA (K and V, or Q and dO) is loaded once; the other pair
+// streams through a two-stage ring.  Every mbarrier wait is bounded as in the
+// forward kernel (timeout status, CTA abort flag, drained copies, freed TMEM).
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+
+#include "fmha_fwd_sm103.cuh"
+
+namespace attn {
+namespace bwd {
+
+constexpr int kComputeWarps = 8;
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
+constexpr int kThreads = 320;
+constexpr int kStages = 2;
+constexpr int kVecBytes = kBM * 4;  // lse2 or delta of one 128-row tile
+
+enum : int {
+    BAR_FIXFULL = 0,
+    BAR_FULL = 1,                  // [stage]
+    BAR_EMPTY = BAR_FULL + kStages,
+    BAR_SFULL = BAR_EMPTY + kStages,
+    BAR_DPFULL,
+    BAR_PREADY,                    // dK/dV kernel: P^T in tensor memory (256 arrivals)
+    BAR_DSREADY,                   // dS (or dS^T) in tensor memory (256 arrivals)
+    BAR_ACCDONE,                   // every accumulating MMA completed
+    BAR_MMADONE,                   // teardown
+    BAR_COUNT
+};
+
+// Shared memory: two fixed tiles, two rings of kStages tiles, and (dK/dV) the
+// per-stage lse2 / delta vectors.  1024-byte aligned base.
+template <int kD>
+struct BwdGeo {
+    static_assert(kD == 64 || kD == 128, "head size 64 or 128");
+    static constexpr int kHalves = kD / 64;
+    static constexpr int kTileBytes = kBM * kD * 2;
+    static constexpr int kFix0 = 0;
+    static constexpr int kFix1 = kTileBytes;
+    static constexpr int kRing0 = 2 * kTileBytes;
+    static constexpr int kRing1 = kRing0 + kStages * kTileBytes;
+    static constexpr int kVec = kRing1 + kStages * kTileBytes;  // [stage] {lse2[128], delta[128]}
+    static constexpr int kBar = kVec + kStages * 2 * kVecBytes;
+    static constexpr int kTmemSlot = kBar + BAR_COUNT * 8;
+    static constexpr int kAbort = kTmemSlot + 4;
+    static constexpr int kSmemBytes = kAbort + 4 + 1024;
+    static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
+    // tensor-memory columns
+    static constexpr uint32_t kTmemS = 0;
+    static constexpr uint32_t kTmemDP = 128;
+    static constexpr uint32_t kTmemAcc0 = 256;        // dV (dK/dV kernel) or dQ
+    static constexpr uint32_t kTmemAcc1 = 256 + kD;   // dK
+};
+
+struct BwdParams {
+    int B, Sq, Skv, Hq, Hkv, D;
+    int causal;                 // 0: none; 1: bottom-right; 2: top-left
+    int diag;                   // key j visible from row i iff j <= i + diag (when causal)
+    int sq_pad;                 // rows per (b, h) in the workspace vectors (multiple of 128)
+    float scale;                // softmax scale
+    float scale_log2;           // scale * log2(e)
+    float* lse2;                // [B, Hq, sq_pad]
+    float* delta;               // [B, Hq, sq_pad]
+    uint16_t* dq;               // [B, Sq, Hq, D]
+    uint16_t* dk;               // [B, Skv, Hkv, D]
+    uint16_t* dv;               // [B, Skv, Hkv, D]
+    int n_q_tiles, n_kv_tiles;
+    unsigned int poll_limit;
+};
+
+// 1-d bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16)
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// packed fp32x2: (d0, d1) = (a0 * b + c0, a1 * b + c1)
+__device__ __forceinline__ void ffma2_b(float& d0, float& d1, float a0, float a1, float b, float c0, float c1) {
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %4};\n\t"
+        "mov.b64 rc, {%5, %6};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b), "f"(c0), "f"(c1));
+}
+
+// packed fp32x2: (d0, d1) = (p0 * (x0 - y0), p1 * (x1 - y1))
+__device__ __forceinline__ void fsubmul2(float& d0, float& d1, float p0, float p1, float x0, float x1, float y0,
+                                         float y1) {
+    asm("{\n\t.reg .b64 rp, rx, ry, rd;\n\t"
+        "mov.b64 rp, {%2, %3};\n\t"
+        "mov.b64 rx, {%4, %5};\n\t"
+        "mov.b64 ry, {%6, %7};\n\t"
+        "sub.rn.f32x2 rd, rx, ry;\n\t"
+        "mul.rn.f32x2 rd, rd, rp;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(p0), "f"(p1), "f"(x0), "f"(x1), "f"(y0), "f"(y1));
+}
+
+template <bool kF16>
+__device__ __forceinline__ float widen16(uint16_t x) {
+    if constexpr (kF16) {
+        float f;
+        asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(x));
+        return f;
+    } else {
+        return __uint_as_float(static_cast<uint32_t>(x) << 16);
+    }
+}
+
+// First query row that sees a key of KV tile n (causal), clamped at 0.
+__host__ __device__ __forceinline__ int first_row_for_kv_tile(const BwdParams& p, int n) {
+    if (!p.causal) return 0;
+    const long long r = (long long)n * kBN - p.diag;
+    return r < 0 ? 0 : (r > p.Sq ? p.Sq : static_cast<int>(r));
+}
+
+// Number of KV tiles the query tile starting at row0 visits.
+__host__ __device__ __forceinline__ int kv_tiles_for_rows(const BwdParams& p, int row0) {
+    if (row0 >= p.Sq) return 0;
+    if (!p.causal) return p.n_kv_tiles;
+    const int last_row = row0 + kBM - 1 < p.Sq - 1 ? row0 + kBM - 1 : p.Sq - 1;
+    const long long last_key = (long long)last_row + p.diag;
+    if (last_key < 0) return 0;
+    const long long n = last_key / kBN + 1;
+    return n < p.n_kv_tiles ? static_cast<int>(n) : p.n_kv_tiles;
+}
+
+// ---------------------------------------------------------------- prep
+// One warp per padded row (b, h, i): delta and lse2.
+template <bool kF16, int kD>
+__global__ void __launch_bounds__(256)
+    bwd_prep_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dO, const float* __restrict__ lse,
+                    const BwdParams p) {
+    const long long gw = (long long)blockIdx.x * 8 + threadIdx.x / 32;
+    const int lane = static_cast<int>(threadIdx.x) & 31;
+    const long long total = (long long)p.B * p.Hq * p.sq_pad;
+    if (gw >= total) return;
+    const int i = static_cast<int>(gw % p.sq_pad);
+    const long long bh = gw / p.sq_pad;
+    const int h = static_cast<int>(bh % p.Hq), b = static_cast<int>(bh / p.Hq);
+    float acc = 0.f;
+    if (i < p.Sq) {
+        constexpr int kPer = kD / 32;
+        const size_t off = ((static_cast<size_t>(b) * p.Sq + i) * p.Hq + h) * kD + kPer * lane;
+        uint16_t ov[kPer], dv[kPer];
+        if constexpr (kPer == 4) {
+            const uint2 a = *reinterpret_cast<const uint2*>(o + off);
+            const uint2 c = *reinterpret_cast<const uint2*>(dO + off);
+            ov[0] = a.x & 0xFFFF, ov[1] = a.x >> 16, ov[2] = a.y & 0xFFFF, ov[3] = a.y >> 16;
+            dv[0] = c.x & 0xFFFF, dv[1] = c.x >> 16, dv[2] = c.y & 0xFFFF, dv[3] = c.y >> 16;
+        } else {
+            const uint32_t a = *reinterpret_cast<const uint32_t*>(o + off);
+            const uint32_t c = *reinterpret_cast<const uint32_t*>(dO + off);
+            ov[0] = a & 0xFFFF, ov[1] = a >> 16;
+            dv[0] = c & 0xFFFF, dv[1] = c >> 16;
+        }
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) acc += widen16<kF16>(ov[e]) * widen16<kF16>(dv[e]);
+    }
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+    if (lane == 0) {
+        float l2 = INFINITY, dl = 0.f;
+        if (i < p.Sq) {
+            const float l = lse[bh * p.Sq + i];
+            l2 = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
+            dl = acc;
+        }
+        p.lse2[gw] = l2;
+        p.delta[gw] = dl;
+    }
+}
+
+// ---------------------------------------------------------------- shared helpers
+struct Roles {
+    uint8_t* smem;
+    uint32_t sbase;
+    int warp, lane;
+};
+
+// K-major x K-major product over the head dimension: D[128 x 128] = A[128 x kD] B[128 x kD]^T
+template <int kD>
+__device__ __forceinline__ void mma_kmajor(uint32_t d, uint64_t a0, uint64_t b0, uint32_t idesc) {
+#pragma unroll
+    for (int kk = 0; kk < kD / 16; ++kk) {
+        const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
+        mma_bf16_ss(d, a0 + off, b0 + off, idesc, kk > 0 ? 1u : 0u);
+    }
+}
+
+// A from tensor memory (128 lanes x 128 packed 16-bit elements) times an MN-major
+// 128 x kD shared-memory tile: D[128 x kD] (+)= A B.  The packed A is stored as
+// two halves of 64 elements (32 columns each) at columns a_tmem and a_tmem + 64:
+// each elementwise warpgroup packs its half over the start of its own fp32
+// columns, so neither overwrites columns the other is still reading.
+__device__ __forceinline__ void mma_tmem_mn(uint32_t d, uint32_t a_tmem, uint64_t b0, uint32_t idesc,
+                                            bool accumulate) {
+#pragma unroll
+    for (int kk = 0; kk < kBN / 16; ++kk)
+        mma_bf16_ts(d, a_tmem + (kk >> 2) * 64 + (kk & 3) * 8, b0 + static_cast<uint64_t>((kk * 16 * 128) >> 4),
+                    idesc, (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// 64 consecutive fp32 columns of this thread's lane (two x32 loads)
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+    tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+    tmem_ld32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+    tmem_wait_ld_regs(*reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+    tmem_wait_ld_regs(*reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+}
+
+// Accumulator columns [c0, c0 + kD/2) of this thread's lane, times `mul`, to
+// kD/2 16-bit elements at dst (16-byte aligned).
+template <bool kF16, int kD>
+__device__ __forceinline__ void store_acc_half(uint32_t taddr, bool have, float mul, uint16_t* dst, bool write) {
+    constexpr int kN = kD / 2;  // 64 or 32
+    uint32_t a[64];
+    if (have) {
+        if constexpr (kN == 64) {
+            tmem_ld64(taddr, a);
+        } else {
+            tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&a[0]));
+            tmem_wait_ld_regs(*reinterpret_cast<uint32_t(*)[32]>(&a[0]));
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < kN; ++e) a[e] = 0u;
+    }
+    if (!write) return;
+#pragma unroll
+    for (int q = 0; q < kN / 8; ++q) {
+        float f[8];
+#pragma unroll
+        for (int e = 0; e < 8; e += 2)
+            fmul2_b(f[e], f[e + 1], __uint_as_float(a[8 * q + e]), __uint_as_float(a[8 * q + e + 1]), mul);
+        reinterpret_cast<uint4*>(dst)[q] = make_uint4(pack_x2<kF16>(f[0], f[1]), pack_x2<kF16>(f[2], f[3]),
+                                                      pack_x2<kF16>(f[4], f[5]), pack_x2<kF16>(f[6], f[7]));
+    }
+}
+
+// ---------------------------------------------------------------- dK / dV
+// Work item of CTA u: KV tile n = u / (B Hkv) (tiles near the start of the keys
+// have the most query rows under a causal mask and go first), (b, hkv) = u % (B Hkv).
+// tm_a / tm_b: Q and dO (streamed); tm_k / tm_v: K and V (fixed).
+template <bool kF16, int kD>
+__global__ void __launch_bounds__(kThreads, 1)
+    fmha_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                         const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                         const BwdParams p) {
+    using G = BwdGeo<kD>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(smem);
+    const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) / 32, 0);
+    const int lane = static_cast<int>(threadIdx.x) & 31;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + G::kAbort);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::kTmemSlot);
+    auto bar = [&](int i) -> uint32_t { return sbase + G::kBar + 8 * i; };
+
+    const int u = static_cast<int>(blockIdx.x);
+    const int bh = u % (p.B * p.Hkv);
+    const int n = u / (p.B * p.Hkv);
+    const int b = bh / p.Hkv, hkv = bh % p.Hkv;
+    const int group = p.Hq / p.Hkv;
+    const int r0 = first_row_for_kv_tile(p, n);
+    const int t0 = r0 >= p.Sq ? p.n_q_tiles : r0 / kBM;  // no query row sees the tile: no steps
+    const int tiles_per_head = p.n_q_tiles - t0;  // >= 0
+    const int steps = group * tiles_per_head;     // (head, query tile) pairs
+    const unsigned int limit = p.poll_limit;
+
+    if (warp == kLoadWarp && lane == 0) {
+        mbar_init(bar(BAR_FIXFULL), 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar(BAR_FULL + s), 1);
+            mbar_init(bar(BAR_EMPTY + s), 1);
+        }
+        mbar_init(bar(BAR_SFULL), 1);
+        mbar_init(bar(BAR_DPFULL), 1);
+        mbar_init(bar(BAR_PREADY), 32 * kComputeWarps);
+        mbar_init(bar(BAR_DSREADY), 32 * kComputeWarps);
+        mbar_init(bar(BAR_ACCDONE), 1);
+        mbar_init(bar(BAR_MMADONE), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_do);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == kLoadWarp) {
+        // =========================== TMA producer ===========================
+        if (lane == 0 && steps > 0) {
+            const uint64_t pol_fix = l2_policy_evict_first();
+            const uint64_t pol_stream = l2_policy_evict_last();
+            mbar_arrive_expect_tx(bar(BAR_FIXFULL), 2 * G::kTileBytes);
+            for (int h = 0; h < G::kHalves; ++h) {
+                tma_load_4d(sbase + G::kFix0 + h * kHalfBytes, &tm_k, h * 64, hkv, n * kBN, b, bar(BAR_FIXFULL),
+                            pol_fix);
+                tma_load_4d(sbase + G::kFix1 + h * kHalfBytes, &tm_v, h * 64, hkv, n * kBN, b, bar(BAR_FIXFULL),
+                            pol_fix);
+            }
+            int issued = 0;
+            for (int st = 0; st < steps; ++st) {
+                const int s = st % kStages, use = st / kStages;
+                if (use > 0 && !wait_bounded(bar(BAR_EMPTY + s), (use - 1) & 1, abort_flag, limit)) break;
+                const int hq = hkv * group + st / tiles_per_head;
+                const int t = t0 + st % tiles_per_head;
+                mbar_arrive_expect_tx(bar(BAR_FULL + s), 2 * G::kTileBytes + 2 * kVecBytes);
+                for (int h = 0; h < G::kHalves; ++h) {
+                    tma_load_4d(sbase + G::kRing0 + s * G::kTileBytes + h * kHalfBytes, &tm_q, h * 64, hq, t * kBM,
+                                b, bar(BAR_FULL + s), pol_stream);
+                    tma_load_4d(sbase + G::kRing1 + s * G::kTileBytes + h * kHalfBytes, &tm_do, h * 64, hq,
+                                t * kBM, b, bar(BAR_FULL + s), pol_stream);
+                }
+                const size_t vo = (static_cast<size_t>(b) * p.Hq + hq) * p.sq_pad + static_cast<size_t>(t) * kBM;
+                bulk_load(sbase + G::kVec + s * 2 * kVecBytes, p.lse2 + vo, kVecBytes, bar(BAR_FULL + s));
+                bulk_load(sbase + G::kVec + s * 2 * kVecBytes + kVecBytes, p.delta + vo, kVecBytes,
+                          bar(BAR_FULL + s));
+                ++issued;
+            }
+            drain_bounded(bar(BAR_FIXFULL), 0, limit);
+            for (int s = 0; s < kStages; ++s) {
+                const int fills = issued > s ? (issued - 1 - s) / kStages + 1 : 0;
+                if (fills) drain_bounded(bar(BAR_FULL + s), (fills - 1) & 1, limit);
+            }
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        // =========================== MMA issuer =============================
+        constexpr uint32_t idesc_s = idesc_f16kind_f32(kBN, kBM, false, kF16);  // S^T, dP^T
+        constexpr uint32_t idesc_acc = idesc_f16kind_f32(kBN, kD, true, kF16);  // dV, dK
+        const uint64_t k_desc = sdesc_sw128(sbase + G::kFix0, 16, 1024);
+        const uint64_t v_desc = sdesc_sw128(sbase + G::kFix1, 16, 1024);
+        const uint64_t q_k0 = sdesc_sw128(sbase + G::kRing0, 16, 1024);
+        const uint64_t do_k0 = sdesc_sw128(sbase + G::kRing1, 16, 1024);
+        const uint64_t q_mn0 = sdesc_sw128(sbase + G::kRing0, kHalfBytes, 1024);
+        const uint64_t do_mn0 = sdesc_sw128(sbase + G::kRing1, kHalfBytes, 1024);
+        const uint32_t tS = tmem_base + G::kTmemS, tDP = tmem_base + G::kTmemDP;
+        const uint32_t tDV = tmem_base + G::kTmemAcc0, tDK = tmem_base + G::kTmemAcc1;
+        bool ok = steps > 0 && wait_bounded(bar(BAR_FIXFULL), 0, abort_flag, limit);
+        for (int st = 0; ok && st < steps; ++st) {
+            const int s = st % kStages, use = st / kStages;
+            const uint64_t so = static_cast<uint64_t>((s * G::kTileBytes) >> 4);
+            if (!wait_bounded(bar(BAR_FULL + s), use & 1, abort_flag, limit)) break;
+            tc_fence_after();
+            if (elect_one()) {
+                mma_kmajor<kD>(tS, k_desc, q_k0 + so, idesc_s);
+                mma_commit(bar(BAR_SFULL));
+                mma_kmajor<kD>(tDP, v_desc, do_k0 + so, idesc_s);
+                mma_commit(bar(BAR_DPFULL));
+            }
+            __syncwarp();
+            if (!wait_bounded(bar(BAR_PREADY), st & 1, abort_flag, limit)) break;
+            tc_fence_after();
+            if (elect_one()) mma_tmem_mn(tDV, tS, do_mn0 + so, idesc_acc, st > 0);
+            __syncwarp();
+            if (!wait_bounded(bar(BAR_DSREADY), st & 1, abort_flag, limit)) break;
+            tc_fence_after();
+            if (elect_one()) {
+                mma_tmem_mn(tDK, tDP, q_mn0 + so, idesc_acc, st > 0);
+                mma_commit(bar(BAR_EMPTY + s));
+                if (st == steps - 1) mma_commit(bar(BAR_ACCDONE));
+            }
+            __syncwarp();
+        }
+        if (elect_one()) {
+            mma_commit(bar(BAR_MMADONE));
+            drain_bounded(bar(BAR_MMADONE), 0, limit);
+        }
+        __syncwarp();
+    } else {
+        // =========================== elementwise warps ======================
+        const int quarter = warp % 4, half = warp / 4;
+        const int jr = quarter * 32 + lane;  // key within the tile = TMEM lane
+        const int key = n * kBN + jr;
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t tS = tmem_base + lane_off + G::kTmemS + 64 * half;
+        const uint32_t tP = tmem_base + lane_off + G::kTmemS + 64 * half;  // packed over own fp32 columns
+        const uint32_t tDP = tmem_base + lane_off + G::kTmemDP + 64 * half;
+        const uint32_t tDS = tmem_base + lane_off + G::kTmemDP + 64 * half;  // packed over own fp32 columns
+        const float sl2 = p.scale_log2;
+        bool ok = true;
+        for (int st = 0; st < steps; ++st) {
+            const int s = st % kStages, use = st / kStages;
+            const int t = t0 + st % tiles_per_head;
+            // the stage's lse2 / delta have landed (visible to this thread), and S^T is in TMEM
+            const bool got = wait_bounded(bar(BAR_FULL + s), use & 1, abort_flag, limit) &&
+                             wait_bounded(bar(BAR_SFULL), st & 1, abort_flag, limit);
+            if (!__all_sync(0xffffffffu, got)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const float* l2 = reinterpret_cast<const float*>(smem + G::kVec + s * 2 * kVecBytes) + 64 * half;
+            const float* dl = l2 + kBM;
+            uint32_t x[64];
+            tmem_ld64(tS, x);
+            // row i = t*128 + 64*half + c sees this key iff key <= i + diag
+            const int row0 = t * kBM + 64 * half;
+            const int cmin = p.causal ? key - p.diag - row0 : -1;  // first visible column
+            float pv[64];
+#pragma unroll
+            for (int c = 0; c < 64; c += 2) {
+                ffma2_b(pv[c], pv[c + 1], __uint_as_float(x[c]), __uint_as_float(x[c + 1]), sl2, -l2[c], -l2[c + 1]);
+                pv[c] = ex2_approx(pv[c]);
+                pv[c + 1] = ex2_approx(pv[c + 1]);
+            }
+            if (cmin > 0) {
+#pragma unroll
+                for (int c = 0; c < 64; ++c)
+                    if (c < cmin) pv[c] = 0.f;
+            }
+            {
+                uint32_t pk[32];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) pk[c] = pack_x2<kF16>(pv[2 * c], pv[2 * c + 1]);
+                tmem_st16(tP, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+                tmem_st16(tP + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(BAR_PREADY));
+            const bool got2 = wait_bounded(bar(BAR_DPFULL), st & 1, abort_flag, limit);
+            if (!__all_sync(0xffffffffu, got2)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            tmem_ld64(tDP, x);
+            {
+                uint32_t pk[32];
+#pragma unroll
+                for (int c = 0; c < 64; c += 2) {
+                    float d0, d1;
+                    fsubmul2(d0, d1, pv[c], pv[c + 1], __uint_as_float(x[c]), __uint_as_float(x[c + 1]), dl[c],
+                             dl[c + 1]);
+                    pk[c / 2] = pack_x2<kF16>(d0, d1);
+                }
+                tmem_st16(tDS, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+                tmem_st16(tDS + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(BAR_DSREADY));
+        }
+        // epilogue: dV and scale * dK of this key, columns [half kD/2, (half+1) kD/2)
+        bool have = ok && steps > 0;
+        if (have) {
+            const bool got = wait_bounded(bar(BAR_ACCDONE), 0, abort_flag, limit);
+            have = __all_sync(0xffffffffu, got);
+            tc_fence_after();
+        }
+        if (ok) {
+            const bool write = key < p.Skv;
+            const size_t off = ((static_cast<size_t>(b) * p.Skv + (write ? key : 0)) * p.Hkv + hkv) * kD + half * (kD / 2);
+            store_acc_half<kF16, kD>(tmem_base + lane_off + G::kTmemAcc0 + half * (kD / 2), have, 1.f, p.dv + off,
+                                     write);
+            store_acc_half<kF16, kD>(tmem_base + lane_off + G::kTmemAcc1 + half * (kD / 2), have, p.scale,
+                                     p.dk + off, write);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
+
+// ---------------------------------------------------------------- dQ
+// Work item of CTA u: query tile t (last tiles first: under a causal mask they
+// visit the most KV tiles), (b, hq) = u % (B Hq).
+template <bool kF16, int kD>
+__global__ void __launch_bounds__(kThreads, 1)
+    fmha_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                       const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                       const BwdParams p) {
+    using G = BwdGeo<kD>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(smem);
+    const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) / 32, 0);
+    const int lane = static_cast<int>(threadIdx.x) & 31;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + G::kAbort);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::kTmemSlot);
+    auto bar = [&](int i) -> uint32_t { return sbase + G::kBar + 8 * i; };
+
+    const int u = static_cast<int>(blockIdx.x);
+    const int bh = u % (p.B * p.Hq);
+    const int tr = u / (p.B * p.Hq);
+    const int t = p.causal ? p.n_q_tiles - 1 - tr : tr;
+    const int b = bh / p.Hq, hq = bh % p.Hq;
+    const int hkv = hq / (p.Hq / p.Hkv);
+    const int nkv = kv_tiles_for_rows(p, t * kBM);
+    const unsigned int limit = p.poll_limit;
+
+    if (warp == kLoadWarp && lane == 0) {
+        mbar_init(bar(BAR_FIXFULL), 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar(BAR_FULL + s), 1);
+            mbar_init(bar(BAR_EMPTY + s), 1);
+        }
+        mbar_init(bar(BAR_SFULL), 1);
+        mbar_init(bar(BAR_DPFULL), 1);
+        mbar_init(bar(BAR_PREADY), 32 * kComputeWarps);
+        mbar_init(bar(BAR_DSREADY), 32 * kComputeWarps);
+        mbar_init(bar(BAR_ACCDONE), 1);
+        mbar_init(bar(BAR_MMADONE), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_do);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == kLoadWarp) {
+        // =========================== TMA producer ===========================
+        if (lane == 0 && nkv > 0) {
+            const uint64_t pol_fix = l2_policy_evict_first();
+            const uint64_t pol_stream = l2_policy_evict_last();
+            mbar_arrive_expect_tx(bar(BAR_FIXFULL), 2 * G::kTileBytes);
+            for (int h = 0; h < G::kHalves; ++h) {
+                tma_load_4d(sbase + G::kFix0 + h * kHalfBytes, &tm_q, h * 64, hq, t * kBM, b, bar(BAR_FIXFULL),
+                            pol_fix);
+                tma_load_4d(sbase + G::kFix1 + h * kHalfBytes, &tm_do, h * 64, hq, t * kBM, b, bar(BAR_FIXFULL),
+                            pol_fix);
+            }
+            int issued = 0;
+            for (int kt = 0; kt < nkv; ++kt) {
+                const int s = kt % kStages, use = kt / kStages;
+                if (use > 0 && !wait_bounded(bar(BAR_EMPTY + s), (use - 1) & 1, abort_flag, limit)) break;
+                mbar_arrive_expect_tx(bar(BAR_FULL + s), 2 * G::kTileBytes);
+                for (int h = 0; h < G::kHalves; ++h) {
+                    tma_load_4d(sbase + G::kRing0 + s * G::kTileBytes + h * kHalfBytes, &tm_k, h * 64, hkv, kt * kBN,
+                                b, bar(BAR_FULL + s), pol_stream);
+                    tma_load_4d(sbase + G::kRing1 + s * G::kTileBytes + h * kHalfBytes, &tm_v, h * 64, hkv, kt * kBN,
+                                b, bar(BAR_FULL + s), pol_stream);
+                }
+                ++issued;
+            }
+            drain_bounded(bar(BAR_FIXFULL), 0, limit);
+            for (int s = 0; s < kStages; ++s) {
+                const int fills = issued > s ? (issued - 1 - s) / kStages + 1 : 0;
+                if (fills) drain_bounded(bar(BAR_FULL + s), (fills - 1) & 1, limit);
+            }
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        // =========================== MMA issuer =============================
+        constexpr uint32_t idesc_s = idesc_f16kind_f32(kBM, kBN, false, kF16);  // S, dP
+        constexpr uint32_t idesc_acc = idesc_f16kind_f32(kBM, kD, true, kF16);  // dQ
+        const uint64_t q_desc = sdesc_sw128(sbase + G::kFix0, 16, 1024);
+        const uint64_t do_desc = sdesc_sw128(sbase + G::kFix1, 16, 1024);
+        const uint64_t k_k0 = sdesc_sw128(sbase + G::kRing0, 16, 1024);
+        const uint64_t v_k0 = sdesc_sw128(sbase + G::kRing1, 16, 1024);
+        const uint64_t k_mn0 = sdesc_sw128(sbase + G::kRing0, kHalfBytes, 1024);
+        const uint32_t tS = tmem_base + G::kTmemS, tDP = tmem_base + G::kTmemDP;
+        const uint32_t tDQ = tmem_base + G::kTmemAcc0;
+        bool ok = nkv > 0 && wait_bounded(bar(BAR_FIXFULL), 0, abort_flag, limit);
+        for (int kt = 0; ok && kt < nkv; ++kt) {
+            const int s = kt % kStages, use = kt / kStages;
+            const uint64_t so = static_cast<uint64_t>((s * G::kTileBytes) >> 4);
+            if (!wait_bounded(bar(BAR_FULL + s), use & 1, abort_flag, limit)) break;
+            tc_fence_after();
+            if (elect_one()) {
+                mma_kmajor<kD>(tS, q_desc, k_k0 + so, idesc_s);
+                mma_commit(bar(BAR_SFULL));
+                mma_kmajor<kD>(tDP, do_desc, v_k0 + so, idesc_s);
+                mma_commit(bar(BAR_DPFULL));
+            }
+            __syncwarp();
+            if (!wait_bounded(bar(BAR_DSREADY), kt & 1, abort_flag, limit)) break;
+            tc_fence_after();
+            if (elect_one()) {
+                mma_tmem_mn(tDQ, tDP, k_mn0 + so, idesc_acc, kt > 0);
+                mma_commit(bar(BAR_EMPTY + s));
+                if (kt == nkv - 1) mma_commit(bar(BAR_ACCDONE));
+            }
+            __syncwarp();
+        }
+        if (elect_one()) {
+            mma_commit(bar(BAR_MMADONE));
+            drain_bounded(bar(BAR_MMADONE), 0, limit);
+        }
+        __syncwarp();
+    } else {
+        // =========================== elementwise warps ======================
+        const int quarter = warp % 4, half = warp / 4;
+        const int r = quarter * 32 + lane;  // row within the tile = TMEM lane
+        const int row = t * kBM + r;
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t tS = tmem_base + lane_off + G::kTmemS + 64 * half;
+        const uint32_t tDP = tmem_base + lane_off + G::kTmemDP + 64 * half;
+        const uint32_t tDS = tmem_base + lane_off + G::kTmemDP + 64 * half;  // packed over own fp32 columns
+        const size_t vo = (static_cast<size_t>(b) * p.Hq + hq) * p.sq_pad + row;  // row < sq_pad
+        const float neg_l2 = -p.lse2[vo];
+        const float dlt = p.delta[vo];
+        const float sl2 = p.scale_log2;
+        // last visible key of this row (keys past Skv are masked too)
+        const long long lim_ll = p.causal ? min((long long)row + p.diag, (long long)p.Skv - 1) : (long long)p.Skv - 1;
+        const int lim = static_cast<int>(lim_ll < -1 ? -1 : lim_ll);
+        bool ok = true;
+        for (int kt = 0; kt < nkv; ++kt) {
+            const bool got = wait_bounded(bar(BAR_SFULL), kt & 1, abort_flag, limit);
+            if (!__all_sync(0xffffffffu, got)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t x[64];
+            tmem_ld64(tS, x);
+            float pv[64];
+#pragma unroll
+            for (int c = 0; c < 64; c += 2) {
+                ffma2_bc(pv[c], pv[c + 1], __uint_as_float(x[c]), __uint_as_float(x[c + 1]), sl2, neg_l2);
+                pv[c] = ex2_approx(pv[c]);
+                pv[c + 1] = ex2_approx(pv[c + 1]);
+            }
+            const int nvis = lim - (kt * kBN + 64 * half) + 1;  // visible columns of this half
+            if (nvis < 64) {
+#pragma unroll
+                for (int c = 0; c < 64; ++c)
+                    if (c >= nvis) pv[c] = 0.f;
+            }
+            const bool got2 = wait_bounded(bar(BAR_DPFULL), kt & 1, abort_flag, limit);
+            if (!__all_sync(0xffffffffu, got2)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            tmem_ld64(tDP, x);
+            {
+                uint32_t pk[32];
+#pragma unroll
+                for (int c = 0; c < 64; c += 2) {
+                    float d0, d1;
+                    fsubmul2(d0, d1, pv[c], pv[c + 1], __uint_as_float(x[c]), __uint_as_float(x[c + 1]), dlt, dlt);
+                    pk[c / 2] = pack_x2<kF16>(d0, d1);
+                }
+                tmem_st16(tDS, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+                tmem_st16(tDS + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(BAR_DSREADY));
+        }
+        bool have = ok && nkv > 0;
+        if (have) {
+            const bool got = wait_bounded(bar(BAR_ACCDONE), 0, abort_flag, limit);
+            have = __all_sync(0xffffffffu, got);
+            tc_fence_after();
+        }
+        if (ok) {
+            const bool write = row < p.Sq;
+            const size_t off = ((static_cast<size_t>(b) * p.Sq + (write ? row : 0)) * p.Hq + hq) * kD + half * (kD / 2);
+            store_acc_half<kF16, kD>(tmem_base + lane_off + G::kTmemAcc0 + half * (kD / 2), have, p.scale,
+                                     p.dq + off, write);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
+
+}  // namespace bwd
+}  // namespace attn

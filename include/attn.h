@@ -134,6 +134,45 @@ attn_status_t attn_fwd_splitkv_noalloc(const void* q, const void* k, const void*
                                        float* lse, int B, int Sq, int Skv, int Hq, int Hkv, int D,
                                        int causal, float scale, cudaStream_t stream);
 
+/*
+ * attn_bwd -- gradients of the attention forward: given dO, the gradient of
+ * L = sum dO * O, with O = softmax(scale * Q K^T [+ mask]) V as in attn_fwd
+ * (the Pallas page, attention_mgpu.py, `_attention_bwd`):
+ *   P = exp(scale * Q K^T - LSE) (masked pairs 0), delta = rowsum(O * dO),
+ *   dP = dO V^T, dS = P * (dP - delta),
+ *   dQ = scale * dS K,  dK = scale * dS^T Q,  dV = P^T dO,
+ * with dK and dV summed over the query heads that share a key/value head.
+ *
+ * q, k, v   device pointers, the forward's inputs (layouts as attn_fwd).
+ * o         device pointer, [B, Sq, Hq, D]: the forward's output.
+ * lse       device pointer, fp32 [B, Hq, Sq]: the forward's natural-log LSE
+ *           (-inf for rows that see no key).
+ * dO        device pointer, [B, Sq, Hq, D]: gradient of the output.
+ * dq        device pointer, [B, Sq, Hq, D]     (written)
+ * dk, dv    device pointers, [B, Skv, Hkv, D]  (written; every element, zero for
+ *           keys no query row sees)
+ * B .. scale  as attn_fwd (the same causal mode and scale as the forward call;
+ *           the page's backward has no mask, this one applies the forward's).
+ * dtype     ATTN_DTYPE_BF16 or ATTN_DTYPE_F16: the element type of q, k, v, o,
+ *           dO, dq, dk and dv.
+ * workspace device pointer, 256-byte aligned, of at least
+ *           attn_bwd_workspace_size bytes (per-row delta and base-2 LSE);
+ *           scratch, contents undefined before and after the call.
+ *
+ * Arithmetic: operands and P, dS in the element type, fp32 accumulation in
+ * tensor memory, fp32 delta; outputs rounded to nearest even once.
+ * Ownership: the caller owns every buffer.  q, k, v, o, dO, dq, dk, dv must be
+ * 16-byte aligned; lse 4-byte aligned.  dq, dk, dv and the workspace must not
+ * overlap any input or each other.  Three kernels are enqueued on `stream`
+ * (prep, dK/dV, dQ); errors are reported as for attn_fwd (nothing is launched
+ * on any error return; a device-side timeout shows in attn_check_device_status).
+ */
+attn_status_t attn_bwd_workspace_size(int B, int Sq, int Skv, int Hq, int Hkv, int D, size_t* bytes);
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                       const void* dO, void* dq, void* dk, void* dv, int B, int Sq, int Skv, int Hq,
+                       int Hkv, int D, int causal, float scale, int dtype, void* workspace,
+                       size_t workspace_bytes, cudaStream_t stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char* attn_status_str(attn_status_t status);
 

@@ -1,0 +1,227 @@
+"""GPU parity of the backward pass (attn_bwd, through the C ABI) against the fp64
+oracle's gradients of sum(dO * O).
+
+Tolerance.  With u the unit roundoff of the element type (2^-8 for bf16,
+2^-11 for binary16) and rms the root-mean-square of the oracle's gradient tensor
+(over the compared elements):
+    mean |g - g_oracle| <= 1 u rms      |g - g_oracle| <= 40 u rms + 2 u |g_oracle|
+The kernels round P and dS to the element type before each product and the
+outputs once at the end; O (used for delta) arrives rounded too.  Each of those
+roundings moves one term of a gradient sum by at most u of itself, so the error
+of an element is a sum of many independent terms of size <= u |term|: its mean
+over a tensor stays below u rms, and the largest of ~10^5 elements stays well
+below 40 u rms -- plus 2 u of the element itself, for the output's own rounding
+and a dominant term's (elements far above the rms, as in a sparse dv, round on
+their own scale).  A wrong scale, sign, delta or mask moves elements by O(rms),
+hundreds of u.
+
+Inputs.  Most cases hand attn_bwd the oracle's O (correctly rounded) and LSE,
+so they test the backward kernels alone.  delta = rowsum(dO * O) is formed from
+the O it is given (as in the Pallas page's backward); the forward's O may sit
+an ulp off the correctly rounded value (within its own tolerance), and where
+dS = P (dP - delta) cancels exactly -- rows that see a single key -- that ulp is
+the whole of dq and dk.  The forward-to-backward pipeline is checked on shapes
+without such rows (test_bwd_after_gpu_forward and the full-size samples).
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from attention_forward_11_gb300 import inputs
+from parity import to_device
+
+pytestmark = pytest.mark.gpu
+
+U = {"bf16": 2.0 ** -8, "f16": 2.0 ** -11}
+MEAN_U, MAX_U, REL_U = 1.0, 40.0, 2.0
+FLOOR = 0.02  # fraction of one term's size below which a tensor's rms is not trusted
+
+
+def problem(B, Sq, Skv, Hq, Hkv, D, seed, dtype="bf16"):
+    q, k, v = inputs.make_qkv(B, Sq, Skv, Hq, Hkv, D, seed=seed, dtype=dtype)
+    do = inputs.normal_bf16(q.shape, 1.0, seed, 3, dtype)
+    return q, k, v, do
+
+
+def oracle_forward_bits(q, k, v, causal, scale, dtype="bf16"):
+    """The forward's outputs as attn_bwd takes them, from the oracle: O correctly
+    rounded to the element type (16-bit patterns) and the fp32 LSE."""
+    o, lse = oracle.attn_full(q, k, v, causal, scale, f16=dtype == "f16")
+    if dtype == "f16":
+        o_bits = oracle.round_f16(o).astype(np.float16).view(np.uint16)
+    else:
+        o_bits = inputs.f32_to_bf16_bits(oracle.round_bf16(o).astype(np.float32))
+    return np.ascontiguousarray(o_bits), lse.astype(np.float32)
+
+
+def gpu_grads(q, k, v, do, causal, scale, dtype="bf16", raw=False, fwd="oracle"):
+    """dq, dk, dv from attn_bwd (fp64 numpy, or the device tensors with raw=True).
+    fwd="oracle": O and LSE are the oracle's (O correctly rounded), which tests
+    the backward kernels on exact inputs; fwd="gpu": they come from attn_fwd, the
+    pipeline a training step runs."""
+    import torch
+    import attention_forward_11_gb300 as fa
+    tq, tk, tv, tdo = (to_device(x, dtype) for x in (q, k, v, do))
+    if fwd == "gpu":
+        o, lse = fa.attn_fwd(tq, tk, tv, causal=int(causal), scale=scale)
+    else:
+        o_bits, lse_np = oracle_forward_bits(q, k, v, causal, scale, dtype)
+        o, lse = to_device(o_bits, dtype), torch.from_numpy(lse_np).cuda()
+    dq, dk, dv = fa.attn_bwd(tq, tk, tv, o, lse, tdo, causal=int(causal), scale=scale)
+    assert fa.attn_check_device_status() == fa.ATTN_OK
+    if raw:
+        return dq, dk, dv
+    out = tuple(t.float().double().cpu().numpy() for t in (dq, dk, dv))
+    torch.cuda.synchronize()
+    return out
+
+
+def term_sizes(q, k, v, do, scale, dtype="bf16"):
+    """Natural size of one term of each gradient sum, from the inputs: a dS K
+    term of dq is ~ scale |dP| |k| with |dP| ~ sqrt(D) |dO| |v| (likewise dk with
+    |q|); a term of dv is ~ |dO|."""
+    w = oracle.f16_bits_to_f64 if dtype == "f16" else oracle.bf16_bits_to_f64
+    rq, rk, rv, rdo = (float(np.sqrt(np.mean(w(x) ** 2))) for x in (q, k, v, do))
+    dp = math.sqrt(q.shape[-1]) * rdo * rv
+    return scale * dp * rk, scale * dp * rq, rdo
+
+
+def compare(got, ref, dtype, what, terms):
+    """Errors are measured against each tensor's rms, floored at 2 % of the size
+    of one term of its sums (`terms`).  With dO = 0 every gradient must be
+    exactly zero."""
+    u = U[dtype]
+    for name, g, r, term in zip(("dq", "dk", "dv"), got, ref, terms):
+        assert np.all(np.isfinite(g)), f"{what} {name}: non-finite"
+        if term == 0.0:
+            assert np.all(g == 0.0), f"{what} {name}: expected zeros"
+            continue
+        norm = max(float(np.sqrt(np.mean(r ** 2))) if r.size else 0.0, FLOOR * term)
+        err = np.abs(g - r)
+        assert err.mean() <= MEAN_U * u * norm, f"{what} {name}: mean err {err.mean() / norm:.3e} rms"
+        excess = err - REL_U * u * np.abs(r)
+        assert excess.max() <= MAX_U * u * norm, f"{what} {name}: max err {excess.max() / norm:.3e} rms"
+
+
+def check(q, k, v, do, causal, scale, what, dtype="bf16", fwd="oracle"):
+    compare(gpu_grads(q, k, v, do, causal, scale, dtype=dtype, fwd=fwd),
+            oracle.attn_bwd(q, k, v, do, causal, scale, f16=dtype == "f16"), dtype, what,
+            term_sizes(q, k, v, do, scale, dtype))
+
+
+CASES = [
+    # B, Sq, Skv, Hq, Hkv, D, causal
+    (1, 256, 256, 2, 2, 128, 0),
+    (1, 256, 256, 2, 2, 128, 1),
+    (1, 300, 300, 4, 2, 128, 1),      # ragged tail, GQA group 2
+    (2, 200, 333, 4, 1, 128, 1),      # Sq < Skv, bottom-right, group 4
+    (1, 333, 200, 2, 1, 128, 1),      # Sq > Skv: rows that see no key
+    (1, 200, 333, 2, 2, 128, 2),      # top-left, keys no row sees
+    (1, 129, 517, 3, 3, 128, 0),
+    (1, 1000, 1000, 2, 1, 128, 0),
+    (1, 384, 384, 2, 2, 64, 1),       # head size 64
+    (1, 250, 390, 4, 2, 64, 2),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "B{}_Sq{}_Skv{}_H{}-{}_D{}_c{}".format(*c))
+def test_bwd_matches_oracle(case):
+    *shape, causal = case
+    q, k, v, do = problem(*shape, seed=sum(case))
+    scale = 1 / math.sqrt(shape[5])
+    check(q, k, v, do, causal, scale, str(case))
+
+
+@pytest.mark.parametrize("case", [(1, 256, 256, 2, 2, 128, 1), (2, 200, 333, 4, 1, 128, 1),
+                                  (1, 1000, 1000, 2, 1, 128, 0), (1, 384, 384, 2, 2, 64, 1)],
+                         ids=lambda c: "B{}_Sq{}_Skv{}_H{}-{}_D{}_c{}".format(*c))
+def test_bwd_after_gpu_forward(case):
+    """O and LSE from attn_fwd, as a training step runs them."""
+    *shape, causal = case
+    q, k, v, do = problem(*shape, seed=sum(case) + 1)
+    check(q, k, v, do, causal, 1 / math.sqrt(shape[5]), str(case), fwd="gpu")
+
+
+@pytest.mark.parametrize("case", [(1, 300, 300, 2, 1, 128, 1), (1, 200, 260, 2, 2, 64, 0)])
+def test_bwd_f16_matches_oracle(case):
+    *shape, causal = case
+    q, k, v, do = problem(*shape, seed=sum(case), dtype="f16")
+    scale = 1 / math.sqrt(shape[5])
+    check(q, k, v, do, causal, scale, str(case), dtype="f16")
+
+
+@pytest.mark.parametrize("causal", [0, 1, 2])
+@pytest.mark.parametrize("Sq,Skv", [(1, 300), (300, 1), (1, 1), (7, 5)])
+def test_bwd_degenerate_lengths(Sq, Skv, causal):
+    q, k, v, do = problem(2, Sq, Skv, 4, 2, 128, seed=Sq + 3 * Skv + causal)
+    scale = 0.125
+    check(q, k, v, do, causal, scale, f"Sq={Sq} Skv={Skv} causal={causal}")
+
+
+def test_bwd_many_tiny_batch_entries():
+    q, k, v, do = problem(64, 5, 9, 2, 1, 128, seed=81)
+    for causal in (0, 1, 2):
+        check(q, k, v, do, causal, 0.1, f"B=64 causal={causal}")
+
+
+def test_bwd_exact_zeros():
+    """Keys that no row sees (top-left mask, Skv > Sq) get dk = dv = 0 exactly;
+    rows that see no key (bottom-right mask, Sq > Skv) get dq = 0 exactly."""
+    q, k, v, do = problem(1, 130, 400, 2, 1, 128, seed=82)
+    dq, dk, dv = gpu_grads(q, k, v, do, 2, 0.1)
+    assert np.all(dk[:, 130:] == 0.0) and np.all(dv[:, 130:] == 0.0)
+    assert np.abs(dk[:, :130]).max() > 0 and np.abs(dv[:, :130]).max() > 0
+    q, k, v, do = problem(1, 400, 130, 2, 1, 128, seed=83)
+    dq, dk, dv = gpu_grads(q, k, v, do, 1, 0.1)
+    assert np.all(dq[:, : 400 - 130] == 0.0)
+    assert np.abs(dq[:, 400 - 130:]).max() > 0
+
+
+def test_bwd_zero_output_gradient():
+    q, k, v, do = problem(1, 300, 300, 2, 2, 128, seed=84)
+    do = np.zeros_like(do)
+    for g in gpu_grads(q, k, v, do, 1, 0.1):
+        assert np.all(g == 0.0)
+
+
+def test_bwd_is_deterministic():
+    """No atomics: two calls give bit-identical gradients."""
+    import torch
+    q, k, v, do = problem(2, 700, 700, 4, 2, 128, seed=85)
+    a = gpu_grads(q, k, v, do, 1, 0.1, raw=True)
+    b = gpu_grads(q, k, v, do, 1, 0.1, raw=True)
+    for x, y in zip(a, b):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+
+
+def _sampled(shape, causal, seed, n_rows, kv_pairs, dtype="bf16"):
+    B, Sq, Skv, Hq, Hkv, D = shape
+    q, k, v, do = problem(*shape, seed=seed, dtype=dtype)
+    scale = 1 / math.sqrt(D)
+    dq, dk, dv = gpu_grads(q, k, v, do, causal, scale, dtype=dtype, fwd="gpu")
+    rows = inputs.sample_rows(B, Hq, Sq, n_rows, seed)
+    ref_dq = oracle.attn_bwd_dq_rows(q, k, v, do, rows, causal, scale, f16=dtype == "f16")
+    got_dq = np.array([dq[b, i, h] for b, h, i in rows])
+    rng = np.random.default_rng(seed)
+    keys = []
+    for b, g in kv_pairs:
+        js = {0, 1, 127, 128, Skv // 2, Skv - 129, Skv - 128, Skv - 1}
+        js.update(rng.integers(0, Skv, 12).tolist())
+        keys += [(b, g, j) for j in sorted(js) if 0 <= j < Skv]
+    ref_dk, ref_dv = oracle.attn_bwd_dkv_keys(q, k, v, do, keys, causal, scale, f16=dtype == "f16")
+    got_dk = np.array([dk[b, j, g] for b, g, j in keys])
+    got_dv = np.array([dv[b, j, g] for b, g, j in keys])
+    compare((got_dq, got_dk, got_dv), (ref_dq, ref_dk, ref_dv), dtype, f"{shape} sampled",
+            term_sizes(q, k, v, do, scale, dtype))
+
+
+def test_bwd_headline_shape_sampled():
+    """B=4, H=16, S=4096, D=128, causal (the forward's headline shape): sampled
+    dq rows and dk/dv keys of two (batch, head) pairs against the oracle."""
+    _sampled((4, 4096, 4096, 16, 16, 128), 1, seed=86, n_rows=48, kv_pairs=[(0, 0), (3, 15)])
+
+
+def test_bwd_gqa_sampled():
+    _sampled((1, 2048, 2048, 8, 2, 128), 1, seed=87, n_rows=32, kv_pairs=[(0, 1)])

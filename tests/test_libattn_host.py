@@ -139,3 +139,46 @@ def test_fwd_ex_validates_like_attn_fwd(lib, dtype):
     assert fa.attn_fwd_ex_ptr(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Sq"], a["Skv"],
                               a["Hq"], a["Hkv"], a["D"], a["causal"], a["scale"], dtype,
                               0) == fa.ATTN_ERR_UNSUPPORTED
+
+
+# ---- backward: argument checks (fake addresses, nothing launched)
+BWD = dict(q=Q, k=K, v=V, o=O, lse=L, do=0x6000000, dq=0x7000000, dk=0x8000000, dv=0x9000000,
+           B=1, Sq=256, Skv=256, Hq=2, Hkv=2, D=128, causal=1, scale=0.088, dtype=0,
+           ws=0xA000000, ws_bytes=1 << 20, stream=0)
+
+
+def call_bwd(**over):
+    a = {**BWD, **over}
+    return fa.attn_bwd_ptr(a["q"], a["k"], a["v"], a["o"], a["lse"], a["do"], a["dq"], a["dk"],
+                           a["dv"], a["B"], a["Sq"], a["Skv"], a["Hq"], a["Hkv"], a["D"],
+                           a["causal"], a["scale"], a["dtype"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("over", [
+    dict(q=0), dict(k=0), dict(v=0), dict(o=0), dict(lse=0), dict(do=0), dict(dq=0), dict(dk=0),
+    dict(dv=0), dict(ws=0),
+    dict(B=0), dict(Sq=0), dict(Skv=-1), dict(Hq=3, Hkv=2), dict(causal=3), dict(dtype=2),
+    dict(scale=0.0), dict(scale=math.nan),
+    dict(q=Q + 8), dict(do=0x6000000 + 4), dict(dq=0x7000000 + 2), dict(dk=0x8000000 + 8),
+    dict(lse=L + 2), dict(ws=0xA000000 + 16), dict(ws_bytes=1024),
+    dict(dq=Q), dict(dk=K + 256), dict(dv=0x6000000), dict(dk=0x9000000), dict(ws=0x7000000),
+    dict(dq=L),
+], ids=lambda d: ",".join(f"{k}={v}" for k, v in d.items()))
+def test_bwd_invalid_arguments_rejected(lib, over):
+    assert call_bwd(**over) == fa.ATTN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("D", [32, 96, 256])
+def test_bwd_other_head_dims_unsupported(lib, D):
+    assert call_bwd(D=D) == fa.ATTN_ERR_UNSUPPORTED
+
+
+def test_bwd_workspace_size(lib):
+    # two fp32 vectors of B * Hq * (Sq rounded up to 128) entries, each rounded up to 256 bytes
+    assert fa.attn_bwd_workspace_size(1, 256, 256, 2, 2, 128) == 2 * 2 * 256 * 4
+    assert fa.attn_bwd_workspace_size(3, 129, 7, 5, 1, 64) == 2 * 3 * 5 * 256 * 4
+    assert fa.attn_bwd_workspace_size(1, 1, 1, 1, 1, 128) == 2 * 512
+    assert lib.attn_bwd_workspace_size(1, 256, 256, 2, 2, 128, None) == fa.ATTN_ERR_INVALID_ARG
+    with pytest.raises(fa.AttnError) as e:
+        fa.attn_bwd_workspace_size(1, 256, 256, 3, 2, 128)
+    assert e.value.status == fa.ATTN_ERR_INVALID_ARG
