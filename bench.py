@@ -12,6 +12,9 @@ inside its timed region.  `roofline` relates the kernel to the measured dense
 bf16 tensor peak.  `cpu_baseline` times the fp64 oracle on a bounded sample of
 the same workload on the host cores.
 
+--path bwd times attn_bwd instead (one step = the gradients dq, dk, dv of one
+forward, 2.5x its FLOPs); it prints no cpu_baseline.
+
 Under torchrun (N > 1) every rank runs an independent replica of the workload
 on its own GPU (the forward pass has no exchange step); the max over ranks of
 the timed region divides the work of all ranks.
@@ -33,6 +36,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd TFLOP/s (bf16, causal FLOPs halved) and % of GB300 dense bf16 peak"
+METRIC_BWD = "attention bwd TFLOP/s (2.5x the forward's FLOPs, causal halved)"
 UNIT = "TFLOP/s"
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 256 << 20
@@ -68,10 +72,16 @@ def load_peaks():
         return FALLBACK_BF16_TFLOPS, "fallback"
 
 
+FWD_KERNEL_SOURCES = ("fmha_fwd_sm103.cuh", "sm103_ptx.cuh")
+
+
 def kernel_source_digest() -> str:
+    """Digest of the forward kernel's sources (its template and the PTX wrappers
+    it is built from): a committed DRAM-traffic figure is used only while it
+    matches the kernel the bench runs."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "attention_forward_11_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in FWD_KERNEL_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
@@ -291,10 +301,34 @@ def run_ours(args, w):
     ws_bytes = 0
     if args.path == "splitkv":  # the caller's scratch, allocated once outside the timed region
         ws_bytes = fa.attn_fwd_splitkv_workspace_size(w.B, w.Sq, w.Skv, w.Hq, w.Hkv, w.D, w.causal)
+    elif args.path == "bwd":
+        ws_bytes = fa.attn_bwd_workspace_size(w.B, w.Sq, w.Skv, w.Hq, w.Hkv, w.D)
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    dtype_code = fa.ATTN_DTYPE_F16 if args.dtype == "f16" else fa.ATTN_DTYPE_BF16
+    if args.path == "bwd":
+        # the backward step's other inputs: the forward's O and LSE, and a seeded dO
+        st = fa.attn_fwd_ex_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                w.B, w.Sq, w.Skv, w.Hq, w.Hkv, w.D, w.causal, w.scale, dtype_code, sh)
+        if st != fa.ATTN_OK:
+            raise fa.AttnError(st, "attn_fwd_ex")
+        dop = pinned(inputs.normal_bf16(q_h.shape, 1.0, rank, 3, args.dtype))
+        do = dop.to(dev)
+        op = torch.empty(o.shape, dtype=tdtype).pin_memory()
+        op.copy_(o)
+        lsep = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+        lsep.copy_(lse)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        dq_h = torch.empty(dq.shape, dtype=tdtype).pin_memory()
+        dk_h = torch.empty(dk.shape, dtype=tdtype).pin_memory()
+        dv_h = torch.empty(dv.shape, dtype=tdtype).pin_memory()
 
     def step():
-        if args.path == "splitkv":
+        if args.path == "bwd":
+            st = fa.attn_bwd_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                 do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), w.B, w.Sq,
+                                 w.Skv, w.Hq, w.Hkv, w.D, w.causal, w.scale, dtype_code, ws.data_ptr(),
+                                 ws_bytes, sh)
+        elif args.path == "splitkv":
             st = fa.attn_fwd_splitkv_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                          lse.data_ptr(), w.B, w.Sq, w.Skv, w.Hq, w.Hkv, w.D,
                                          w.causal, w.scale, ws.data_ptr(), ws_bytes, sh)
@@ -351,6 +385,15 @@ def run_ours(args, w):
         q.copy_(qp, non_blocking=True)
         k.copy_(kp, non_blocking=True)
         v.copy_(vp, non_blocking=True)
+        if args.path == "bwd":
+            o.copy_(op, non_blocking=True)
+            lse.copy_(lsep, non_blocking=True)
+            do.copy_(dop, non_blocking=True)
+            step()
+            dq_h.copy_(dq, non_blocking=True)
+            dk_h.copy_(dk, non_blocking=True)
+            dv_h.copy_(dv, non_blocking=True)
+            continue
         step()
         o_h.copy_(o, non_blocking=True)
         lse_h.copy_(lse, non_blocking=True)
@@ -364,31 +407,42 @@ def run_ours(args, w):
     if rank != 0:
         return
 
-    flops = metric_flops(w)
+    bwd = args.path == "bwd"
+    # backward: 2.5 x the forward's FLOPs (five products of 2 D FLOPs per pair, not two)
+    fl_mult = 2.5 if bwd else 1.0
+    flops = int(fl_mult * metric_flops(w))
     value = job_tflops(world, flops, args.steps, kernel_s)
     e2e_value = job_tflops(world, flops, e2e_steps, e2e_s)
     peak, peak_kind = load_peaks()
-    exact = exact_flops(w)
+    exact = int(fl_mult * exact_flops(w))
     mean_launch_s = kernel_s / args.steps
     achieved = exact / mean_launch_s / 1e12
     bytes_in = q.numel() * 2 + k.numel() * 2 + v.numel() * 2
     bytes_out = o.numel() * 2 + lse.numel() * 4
+    if bwd:
+        bytes_in += o.numel() * 2 + lse.numel() * 4 + do.numel() * 2
+        bytes_out = dq.numel() * 2 + dk.numel() * 2 + dv.numel() * 2
+    entry = {"fwd": "attn_fwd_ex" if args.dtype == "f16" else "attn_fwd",
+             "splitkv": "attn_fwd_splitkv", "bwd": "attn_bwd"}[args.path]
 
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": METRIC_BWD if bwd else METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * mean_launch_s, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": args.dtype, "data": "synthetic",
         "config": {**w.as_dict(), "parallelism": "replicas" if world > 1 else "single",
-                   "entry_point": "attn_fwd_splitkv" if args.path == "splitkv" else "attn_fwd",
+                   "entry_point": entry,
                    "workspace_bytes": ws_bytes,
                    "l2": "flushed between steps (256 MiB write); inputs also exceed L2",
                    "metric_flops_per_step": flops, "exact_visible_pair_flops_per_step": exact,
                    "pct_of_peak": 100.0 * value / peak},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": load_traffic(w.name),
+                     "frac": achieved / peak,
+                     "traffic": None if bwd else load_traffic(w.name),
                      "peak_source": f"bf16_tflops (burst) of {peak_kind}",
-                     "kernel": "attn::fmha_fwd_kernel",
-                     "algorithmic_unit": "4*D FLOPs per visible (q-row, key, q-head)"},
+                     "kernel": ("attn_bwd step: bwd_prep_kernel + fmha_bwd_dkdv_kernel + "
+                                "fmha_bwd_dq_kernel") if bwd else "attn::fmha_fwd_kernel",
+                     "algorithmic_unit": ("10*D FLOPs per visible (q-row, key, q-head)" if bwd else
+                                          "4*D FLOPs per visible (q-row, key, q-head)")},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": bytes_in,
                 "d2h_bytes_per_step": bytes_out, "steps": e2e_steps},
         "gpu_launches": int(launches),
@@ -397,7 +451,7 @@ def run_ours(args, w):
         "kernel_ms": {"min": min(times_ms), "median": statistics.median(times_ms),
                       "max": max(times_ms)},
     }
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and not bwd:
         tf, dt, n, cores = oracle_sample_rate(w, args.cpu_seconds)
         line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": cores, "kind": "oracle",
                                 "sample": f"{n} random query rows of {w.name} "
@@ -418,8 +472,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--dtype", choices=["bf16", "f16"], default="bf16",
                     help="element type of Q, K, V, O (f16 goes through attn_fwd_ex)")
-    ap.add_argument("--path", choices=["fwd", "splitkv"], default="fwd",
-                    help="entry point timed: attn_fwd, or attn_fwd_splitkv with its workspace")
+    ap.add_argument("--path", choices=["fwd", "splitkv", "bwd"], default="fwd",
+                    help="entry point timed: attn_fwd, attn_fwd_splitkv with its workspace, or "
+                         "attn_bwd (one step = the backward of one forward)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     if args.dtype == "f16" and args.path == "splitkv":
