@@ -111,7 +111,8 @@ def num_threads() -> int:
 
 def attn_rows(q, k, v, rows, causal: int, scale: float, f16: bool = False):
     """fp64 o (len(rows) x D) and lse (len(rows)) for the listed (b, h, i) rows.
-    causal: 0 none, 1 bottom-right (j <= i + Skv - Sq), 2 top-left (j <= i).
+    causal: 0 none, 1 bottom-right (j <= i + Skv - Sq), 2 top-left (j <= i: the
+    Pallas page's `attention_reference` mask, `q_idx >= kv_idx`, for any Sq, Skv).
     f16: the uint16 inputs are IEEE binary16 bit patterns instead of bf16."""
     B, Sq, Skv, Hq, Hkv, D = _check_inputs(q, k, v)
     rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
