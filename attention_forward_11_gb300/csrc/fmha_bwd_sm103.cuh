@@ -52,7 +52,7 @@ enum : int {
     BAR_EMPTY = BAR_FULL + kStages,
     BAR_SFULL = BAR_EMPTY + kStages,
     BAR_DPFULL,
-    BAR_PREADY,                    // dK/dV kernel: P^T in tensor memory (256 arrivals)
+    BAR_PREADY,                    // dK/dV: P^T in tensor memory; dQ: S read out (256 arrivals)
     BAR_DSREADY,                   // dS (or dS^T) in tensor memory (256 arrivals)
     BAR_ACCDONE,                   // every accumulating MMA completed
     BAR_MMADONE,                   // teardown
@@ -276,8 +276,11 @@ __device__ __forceinline__ void store_acc_half(uint32_t taddr, bool have, float 
 }
 
 // ---------------------------------------------------------------- dK / dV
-// Work item of CTA u: KV tile n = u / (B Hkv) (tiles near the start of the keys
-// have the most query rows under a causal mask and go first), (b, hkv) = u % (B Hkv).
+// Work item of CTA u: (b, hkv) = u / n_kv_tiles, KV tile n = u % n_kv_tiles.
+// The CTAs of one head run side by side, so the Q and dO tiles they all stream
+// stay in L2 (a few heads' worth at a time instead of every head's); within a
+// head the tiles near the start of the keys, which see the most query rows
+// under a causal mask, go first.
 // tm_a / tm_b: Q and dO (streamed); tm_k / tm_v: K and V (fixed).
 template <bool kF16, int kD>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -295,8 +298,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bar = [&](int i) -> uint32_t { return sbase + G::kBar + 8 * i; };
 
     const int u = static_cast<int>(blockIdx.x);
-    const int bh = u % (p.B * p.Hkv);
-    const int n = u / (p.B * p.Hkv);
+    const int bh = u / p.n_kv_tiles;
+    const int n = u % p.n_kv_tiles;
     const int b = bh / p.Hkv, hkv = bh % p.Hkv;
     const int group = p.Hq / p.Hkv;
     const int r0 = first_row_for_kv_tile(p, n);
@@ -383,23 +386,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t do_mn0 = sdesc_sw128(sbase + G::kRing1, kHalfBytes, 1024);
         const uint32_t tS = tmem_base + G::kTmemS, tDP = tmem_base + G::kTmemDP;
         const uint32_t tDV = tmem_base + G::kTmemAcc0, tDK = tmem_base + G::kTmemAcc1;
-        bool ok = steps > 0 && wait_bounded(bar(BAR_FIXFULL), 0, abort_flag, limit);
-        for (int st = 0; ok && st < steps; ++st) {
-            const int s = st % kStages, use = st / kStages;
-            const uint64_t so = static_cast<uint64_t>((s * G::kTileBytes) >> 4);
-            if (!wait_bounded(bar(BAR_FULL + s), use & 1, abort_flag, limit)) break;
+        // Issue order S^T_0, dP^T_0, then per step t:
+        //   dV_t, S^T_{t+1}, dK_t, dP^T_{t+1}
+        // so each elementwise phase (P^T_t before dV_t, dS^T_t before dK_t) is
+        // covered by two products.  S^T_{t+1} overwrites P^T_t after dV_t has read
+        // it and dP^T_{t+1} overwrites dS^T_t after dK_t (one thread's tcgen05
+        // MMAs execute in issue order).
+        auto issue_s = [&](int st) -> bool {  // S^T of step st; its stage must have landed
+            const int s = st % kStages;
+            if (!wait_bounded(bar(BAR_FULL + s), (st / kStages) & 1, abort_flag, limit)) return false;
             tc_fence_after();
             if (elect_one()) {
-                mma_kmajor<kD>(tS, k_desc, q_k0 + so, idesc_s);
+                mma_kmajor<kD>(tS, k_desc, q_k0 + static_cast<uint64_t>((s * G::kTileBytes) >> 4), idesc_s);
                 mma_commit(bar(BAR_SFULL));
-                mma_kmajor<kD>(tDP, v_desc, do_k0 + so, idesc_s);
+            }
+            __syncwarp();
+            return true;
+        };
+        auto issue_dp = [&](int st) {
+            const int s = st % kStages;
+            if (elect_one()) {
+                mma_kmajor<kD>(tDP, v_desc, do_k0 + static_cast<uint64_t>((s * G::kTileBytes) >> 4), idesc_s);
                 mma_commit(bar(BAR_DPFULL));
             }
             __syncwarp();
+        };
+        bool ok = steps > 0 && wait_bounded(bar(BAR_FIXFULL), 0, abort_flag, limit) && issue_s(0);
+        if (ok) issue_dp(0);
+        for (int st = 0; ok && st < steps; ++st) {
+            const int s = st % kStages;
+            const uint64_t so = static_cast<uint64_t>((s * G::kTileBytes) >> 4);
             if (!wait_bounded(bar(BAR_PREADY), st & 1, abort_flag, limit)) break;
             tc_fence_after();
             if (elect_one()) mma_tmem_mn(tDV, tS, do_mn0 + so, idesc_acc, st > 0);
             __syncwarp();
+            if (st + 1 < steps && !issue_s(st + 1)) break;
             if (!wait_bounded(bar(BAR_DSREADY), st & 1, abort_flag, limit)) break;
             tc_fence_after();
             if (elect_one()) {
@@ -408,6 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (st == steps - 1) mma_commit(bar(BAR_ACCDONE));
             }
             __syncwarp();
+            if (st + 1 < steps) issue_dp(st + 1);
         }
         if (elect_one()) {
             mma_commit(bar(BAR_MMADONE));
@@ -515,8 +537,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------- dQ
-// Work item of CTA u: query tile t (last tiles first: under a causal mask they
-// visit the most KV tiles), (b, hq) = u % (B Hq).
+// Work item of CTA u: (b, hq) = u / n_q_tiles and its query tile t (last tiles
+// first: under a causal mask they visit the most KV tiles); the CTAs of one
+// head stream the same K/V tiles side by side, out of L2.
 template <bool kF16, int kD>
 __global__ void __launch_bounds__(kThreads, 1)
     fmha_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -533,8 +556,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bar = [&](int i) -> uint32_t { return sbase + G::kBar + 8 * i; };
 
     const int u = static_cast<int>(blockIdx.x);
-    const int bh = u % (p.B * p.Hq);
-    const int tr = u / (p.B * p.Hq);
+    const int bh = u / p.n_q_tiles;
+    const int tr = u % p.n_q_tiles;
     const int t = p.causal ? p.n_q_tiles - 1 - tr : tr;
     const int b = bh / p.Hq, hq = bh % p.Hq;
     const int hkv = hq / (p.Hq / p.Hkv);
@@ -612,19 +635,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t k_mn0 = sdesc_sw128(sbase + G::kRing0, kHalfBytes, 1024);
         const uint32_t tS = tmem_base + G::kTmemS, tDP = tmem_base + G::kTmemDP;
         const uint32_t tDQ = tmem_base + G::kTmemAcc0;
-        bool ok = nkv > 0 && wait_bounded(bar(BAR_FIXFULL), 0, abort_flag, limit);
-        for (int kt = 0; ok && kt < nkv; ++kt) {
-            const int s = kt % kStages, use = kt / kStages;
-            const uint64_t so = static_cast<uint64_t>((s * G::kTileBytes) >> 4);
-            if (!wait_bounded(bar(BAR_FULL + s), use & 1, abort_flag, limit)) break;
+        // Issue order S_0, dP_0, then per KV tile n:
+        //   [S_n read out] S_{n+1}, [dS_n stored] dQ_n, dP_{n+1}
+        // The elementwise warps signal (PREADY) as soon as S_n is in their
+        // registers, so S_{n+1} runs while they form P_n and dS_n; dP_{n+1}
+        // overwrites dS_n only after dQ_n (issue order).
+        auto issue_s = [&](int kt) -> bool {  // S of KV tile kt; its stage must have landed
+            const int s = kt % kStages;
+            if (!wait_bounded(bar(BAR_FULL + s), (kt / kStages) & 1, abort_flag, limit)) return false;
             tc_fence_after();
             if (elect_one()) {
-                mma_kmajor<kD>(tS, q_desc, k_k0 + so, idesc_s);
+                mma_kmajor<kD>(tS, q_desc, k_k0 + static_cast<uint64_t>((s * G::kTileBytes) >> 4), idesc_s);
                 mma_commit(bar(BAR_SFULL));
-                mma_kmajor<kD>(tDP, do_desc, v_k0 + so, idesc_s);
+            }
+            __syncwarp();
+            return true;
+        };
+        auto issue_dp = [&](int kt) {
+            const int s = kt % kStages;
+            if (elect_one()) {
+                mma_kmajor<kD>(tDP, do_desc, v_k0 + static_cast<uint64_t>((s * G::kTileBytes) >> 4), idesc_s);
                 mma_commit(bar(BAR_DPFULL));
             }
             __syncwarp();
+        };
+        bool ok = nkv > 0 && wait_bounded(bar(BAR_FIXFULL), 0, abort_flag, limit) && issue_s(0);
+        if (ok) issue_dp(0);
+        for (int kt = 0; ok && kt < nkv; ++kt) {
+            const int s = kt % kStages;
+            const uint64_t so = static_cast<uint64_t>((s * G::kTileBytes) >> 4);
+            if (kt + 1 < nkv) {
+                if (!wait_bounded(bar(BAR_PREADY), kt & 1, abort_flag, limit)) break;  // S_kt read out
+                if (!issue_s(kt + 1)) break;
+            }
             if (!wait_bounded(bar(BAR_DSREADY), kt & 1, abort_flag, limit)) break;
             tc_fence_after();
             if (elect_one()) {
@@ -633,6 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (kt == nkv - 1) mma_commit(bar(BAR_ACCDONE));
             }
             __syncwarp();
+            if (kt + 1 < nkv) issue_dp(kt + 1);
         }
         if (elect_one()) {
             mma_commit(bar(BAR_MMADONE));
@@ -665,6 +709,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             uint32_t x[64];
             tmem_ld64(tS, x);
+            tc_fence_before();
+            mbar_arrive(bar(BAR_PREADY));  // S may now be overwritten by the next tile's product
             float pv[64];
 #pragma unroll
             for (int c = 0; c < 64; c += 2) {
