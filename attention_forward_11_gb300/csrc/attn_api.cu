@@ -18,6 +18,7 @@
 #include <cuda_runtime.h>
 
 #include "fmha_bwd_sm103.cuh"
+#include "fmha_fwd_d256_sm103.cuh"
 #include "fmha_fwd_sm103.cuh"
 
 namespace {
@@ -90,6 +91,10 @@ bool device_setup(int dev, int* sm_count) {
             !opt_in_smem<attn::PlainSched, true, 64>() || !opt_in_smem<attn::SplitSched, false, 64>() ||
             !opt_in_smem_bwd<false, 128>() || !opt_in_smem_bwd<true, 128>() || !opt_in_smem_bwd<false, 64>() ||
             !opt_in_smem_bwd<true, 64>() ||
+            cudaFuncSetAttribute(attn::d256::fmha_fwd_d256_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 attn::d256::Geo::kSmemBytes) != cudaSuccess ||
+            cudaFuncSetAttribute(attn::d256::fmha_fwd_d256_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 attn::d256::Geo::kSmemBytes) != cudaSuccess ||
             cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
             return false;
         sms[dev] = n;
@@ -109,7 +114,7 @@ attn_status_t check_sizes(int B, int Sq, int Skv, int Hq, int Hkv, int D, int ca
     if (B < 1 || Sq < 1 || Skv < 1 || Hq < 1 || Hkv < 1 || D < 1) return ATTN_ERR_INVALID_ARG;
     if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
     if (causal < 0 || causal > 2) return ATTN_ERR_INVALID_ARG;
-    if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+    if (D != 64 && D != 128 && D != 256) return ATTN_ERR_UNSUPPORTED;
     return ATTN_OK;
 }
 
@@ -189,6 +194,7 @@ size_t workspace_bytes_for(int n_slots, int D) {
 
 void build_split_plan(const attn::FwdParams& p, int sms, SplitPlan* plan) {
     plan->split = false;
+    if (p.D == 256) return;  // head size 256 runs its own one-tile-per-CTA kernel, unsplit
     if (p.n_units < 1 || p.n_units > attn::kMaxPieces) return;
     std::vector<int> W(p.n_units);
     long long T = 0;
@@ -251,6 +257,16 @@ void build_split_plan(const attn::FwdParams& p, int sms, SplitPlan* plan) {
 
 template <bool kF16 = false>
 attn_status_t launch_plain(const CUtensorMap* tm, const attn::FwdParams& p, int sms, cudaStream_t stream) {
+    if (p.D == 256) {
+        // one 128-row query tile per CTA (its O fills half of tensor memory)
+        const long long tiles = (long long)p.B * p.Hq * ((p.Sq + attn::kBM - 1) / attn::kBM);
+        if (tiles > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+        attn::d256::fmha_fwd_d256_kernel<kF16><<<static_cast<unsigned int>(tiles), attn::d256::kThreads,
+                                                 attn::d256::Geo::kSmemBytes, stream>>>(tm[0], tm[1], tm[2], tm[3], p);
+        if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+        return ATTN_OK;
+    }
     // persistent grid: at most one CTA per SM (the CTA holds all 512 TMEM columns)
     const int grid = p.n_units < sms ? p.n_units : sms;
     if (p.D == 64)
@@ -413,6 +429,7 @@ void* static_scratch_address(int dev) {
 // The split plan of build_split_plan, computed in fixed-size storage (no heap).
 void build_split_plan_fixed(const attn::FwdParams& p, int sms, SplitPlan* plan) {
     plan->split = false;
+    if (p.D == 256) return;  // as build_split_plan
     if (p.n_units < 1 || p.n_units > attn::kMaxPieces) return;
     int W[attn::kMaxPieces];
     long long bnd[attn::kMaxSplitCtas + 1];
@@ -516,7 +533,8 @@ attn_status_t launch_bwd(const CUtensorMap* tm, const void* o, const void* dO, c
                          const attn::bwd::BwdParams& p, cudaStream_t stream) {
     using namespace attn::bwd;
     const long long rows = (long long)p.B * p.Hq * p.sq_pad;
-    bwd_prep_kernel<kF16, kD><<<static_cast<unsigned int>((rows + 7) / 8), 256, 0, stream>>>(
+    const long long per_block = 8LL * prep_rows_per_warp<kD>();
+    bwd_prep_kernel<kF16, kD><<<static_cast<unsigned int>((rows + per_block - 1) / per_block), 256, 0, stream>>>(
         static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dO), lse, p);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -538,6 +556,7 @@ extern "C" attn_status_t attn_bwd_workspace_size(int B, int Sq, int Skv, int Hq,
     *bytes = 0;
     const attn_status_t st = check_sizes(B, Sq, Skv, Hq, Hkv, D, 0);
     if (st != ATTN_OK) return st;
+    if (D == 256) return ATTN_ERR_UNSUPPORTED;  // the backward kernels take D <= 128
     *bytes = 2 * bwd_vec_bytes(B, Sq, Hq);
     return ATTN_OK;
 }
@@ -549,7 +568,8 @@ extern "C" attn_status_t attn_bwd(const void* q, const void* k, const void* v, c
     // ---- validation: nothing is launched on any error
     if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !workspace) return ATTN_ERR_INVALID_ARG;
     if (dtype != ATTN_DTYPE_BF16 && dtype != ATTN_DTYPE_F16) return ATTN_ERR_INVALID_ARG;
-    const attn_status_t st = check_sizes(B, Sq, Skv, Hq, Hkv, D, causal);
+    attn_status_t st = check_sizes(B, Sq, Skv, Hq, Hkv, D, causal);
+    if (st == ATTN_OK && D == 256) st = ATTN_ERR_UNSUPPORTED;  // the backward kernels take D <= 128
     if (st == ATTN_ERR_INVALID_ARG) return st;
     if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
     for (const void* ptr : {q, k, v, o, dO, static_cast<const void*>(dq), static_cast<const void*>(dk),

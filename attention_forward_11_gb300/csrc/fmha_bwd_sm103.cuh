@@ -163,48 +163,70 @@ __host__ __device__ __forceinline__ int kv_tiles_for_rows(const BwdParams& p, in
 }
 
 // ---------------------------------------------------------------- prep
-// One warp per padded row (b, h, i): delta and lse2.
+// delta and lse2 of every padded row.  Rows are taken in memory order
+// (b, i, h), so a warp's loads of O and dO are contiguous: each lane loads
+// 16 bytes of each, kD / 8 lanes cover a row, and a warp handles kPrepIters
+// groups of 32 / (kD / 8) rows with all loads issued before the reductions.
+constexpr int kPrepIters = 4;
+template <int kD>
+__host__ __device__ constexpr int prep_rows_per_warp() {
+    return (32 / (kD / 8)) * kPrepIters;
+}
+
 template <bool kF16, int kD>
 __global__ void __launch_bounds__(256)
     bwd_prep_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dO, const float* __restrict__ lse,
                     const BwdParams p) {
-    const long long gw = (long long)blockIdx.x * 8 + threadIdx.x / 32;
+    constexpr int kL = kD / 8;          // lanes per row
+    constexpr int kR = 32 / kL;         // rows per load instruction
     const int lane = static_cast<int>(threadIdx.x) & 31;
-    const long long total = (long long)p.B * p.Hq * p.sq_pad;
-    if (gw >= total) return;
-    const int i = static_cast<int>(gw % p.sq_pad);
-    const long long bh = gw / p.sq_pad;
-    const int h = static_cast<int>(bh % p.Hq), b = static_cast<int>(bh / p.Hq);
-    float acc = 0.f;
-    if (i < p.Sq) {
-        constexpr int kPer = kD / 32;
-        const size_t off = ((static_cast<size_t>(b) * p.Sq + i) * p.Hq + h) * kD + kPer * lane;
-        uint16_t ov[kPer], dv[kPer];
-        if constexpr (kPer == 4) {
-            const uint2 a = *reinterpret_cast<const uint2*>(o + off);
-            const uint2 c = *reinterpret_cast<const uint2*>(dO + off);
-            ov[0] = a.x & 0xFFFF, ov[1] = a.x >> 16, ov[2] = a.y & 0xFFFF, ov[3] = a.y >> 16;
-            dv[0] = c.x & 0xFFFF, dv[1] = c.x >> 16, dv[2] = c.y & 0xFFFF, dv[3] = c.y >> 16;
-        } else {
-            const uint32_t a = *reinterpret_cast<const uint32_t*>(o + off);
-            const uint32_t c = *reinterpret_cast<const uint32_t*>(dO + off);
-            ov[0] = a & 0xFFFF, ov[1] = a >> 16;
-            dv[0] = c & 0xFFFF, dv[1] = c >> 16;
-        }
+    const long long total = (long long)p.B * p.sq_pad * p.Hq;
+    const long long row0 = ((long long)blockIdx.x * 8 + threadIdx.x / 32) * (kR * kPrepIters);
+    uint4 ov[kPrepIters], dv[kPrepIters];
+    long long rr[kPrepIters];
+    bool live[kPrepIters];
 #pragma unroll
-        for (int e = 0; e < kPer; ++e) acc += widen16<kF16>(ov[e]) * widen16<kF16>(dv[e]);
+    for (int it = 0; it < kPrepIters; ++it) {
+        const long long r = row0 + it * kR + lane / kL;  // (b, i, h) in memory order over padded rows
+        rr[it] = r;
+        const int i = r < total ? static_cast<int>((r / p.Hq) % p.sq_pad) : p.Sq;
+        live[it] = i < p.Sq;
+        ov[it] = dv[it] = make_uint4(0u, 0u, 0u, 0u);
+        if (live[it]) {
+            const long long b = r / ((long long)p.sq_pad * p.Hq);
+            const int h = static_cast<int>(r % p.Hq);
+            const size_t off = ((static_cast<size_t>(b) * p.Sq + i) * p.Hq + h) * kD + 8 * (lane % kL);
+            ov[it] = *reinterpret_cast<const uint4*>(o + off);
+            dv[it] = *reinterpret_cast<const uint4*>(dO + off);
+        }
     }
 #pragma unroll
-    for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-    if (lane == 0) {
-        float l2 = INFINITY, dl = 0.f;
-        if (i < p.Sq) {
-            const float l = lse[bh * p.Sq + i];
-            l2 = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
-            dl = acc;
+    for (int it = 0; it < kPrepIters; ++it) {
+        const uint32_t a[4] = {ov[it].x, ov[it].y, ov[it].z, ov[it].w};
+        const uint32_t c[4] = {dv[it].x, dv[it].y, dv[it].z, dv[it].w};
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            acc += widen16<kF16>(static_cast<uint16_t>(a[e] & 0xFFFF)) * widen16<kF16>(static_cast<uint16_t>(c[e] & 0xFFFF));
+            acc += widen16<kF16>(static_cast<uint16_t>(a[e] >> 16)) * widen16<kF16>(static_cast<uint16_t>(c[e] >> 16));
         }
-        p.lse2[gw] = l2;
-        p.delta[gw] = dl;
+#pragma unroll
+        for (int sft = kL / 2; sft > 0; sft >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sft);
+        const long long r = rr[it];
+        if (lane % kL == 0 && r < total) {
+            const long long b = r / ((long long)p.sq_pad * p.Hq);
+            const int i = static_cast<int>((r / p.Hq) % p.sq_pad);
+            const int h = static_cast<int>(r % p.Hq);
+            const size_t w = (static_cast<size_t>(b) * p.Hq + h) * p.sq_pad + i;
+            float l2 = INFINITY, dl = 0.f;
+            if (live[it]) {
+                const float l = lse[(static_cast<size_t>(b) * p.Hq + h) * p.Sq + i];
+                l2 = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
+                dl = acc;
+            }
+            p.lse2[w] = l2;
+            p.delta[w] = dl;
+        }
     }
 }
 

@@ -48,8 +48,9 @@ WORKLOADS = {
                                       q_sigma=4.0),
     "chunked_prefill_gqa_64x8_512x32768": Workload("chunked_prefill_gqa_64x8_512x32768", 1, 64,
                                                    8, 512, 32768, 128, 1),
-    # the headline shape at head size 64 (the Pallas page's benchmark also sweeps D = 64)
+    # the headline shape at head sizes 64 and 256 (the Pallas page's benchmark sweeps 64, 128, 256)
     "mha_causal_4x16x4096_d64": Workload("mha_causal_4x16x4096_d64", 4, 16, 16, 4096, 4096, 64, 1),
+    "mha_causal_4x16x4096_d256": Workload("mha_causal_4x16x4096_d256", 4, 16, 16, 4096, 4096, 256, 1),
 }
 
 HEADLINE = "mha_causal_4x16x4096"

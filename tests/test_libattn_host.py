@@ -69,7 +69,7 @@ def test_invalid_arguments_rejected(lib, over):
     assert call(**over) == fa.ATTN_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("D", [32, 96, 192, 256])
+@pytest.mark.parametrize("D", [32, 96, 192, 320])
 def test_other_head_dims_unsupported(lib, D):
     assert call(D=D) == fa.ATTN_ERR_UNSUPPORTED
 
@@ -110,7 +110,7 @@ def test_splitkv_invalid_arguments_rejected(lib, over):
 
 
 def test_splitkv_other_head_dims_unsupported(lib):
-    assert call_split(D=256) == fa.ATTN_ERR_UNSUPPORTED
+    assert call_split(D=192) == fa.ATTN_ERR_UNSUPPORTED
 
 
 def test_splitkv_workspace_size_argument_checks(lib):
@@ -135,7 +135,7 @@ def test_fwd_ex_validates_like_attn_fwd(lib, dtype):
     assert fa.attn_fwd_ex_ptr(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Sq"], a["Skv"],
                               a["Hq"], a["Hkv"], a["D"], a["causal"], a["scale"], dtype,
                               0) == fa.ATTN_ERR_INVALID_ARG
-    a = {**GOOD, "D": 256}
+    a = {**GOOD, "D": 192}
     assert fa.attn_fwd_ex_ptr(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Sq"], a["Skv"],
                               a["Hq"], a["Hkv"], a["D"], a["causal"], a["scale"], dtype,
                               0) == fa.ATTN_ERR_UNSUPPORTED
@@ -182,3 +182,6 @@ def test_bwd_workspace_size(lib):
     with pytest.raises(fa.AttnError) as e:
         fa.attn_bwd_workspace_size(1, 256, 256, 3, 2, 128)
     assert e.value.status == fa.ATTN_ERR_INVALID_ARG
+    with pytest.raises(fa.AttnError) as e:  # the forward takes D = 256, the backward does not
+        fa.attn_bwd_workspace_size(1, 256, 256, 2, 2, 256)
+    assert e.value.status == fa.ATTN_ERR_UNSUPPORTED
