@@ -33,7 +33,7 @@ extern "C" {
 typedef enum {
     ATTN_OK = 0,
     ATTN_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment, scale or flag; nothing launched */
-    ATTN_ERR_UNSUPPORTED = 2, /* valid request this build does not implement (D not 64/128) */
+    ATTN_ERR_UNSUPPORTED = 2, /* valid request this build does not implement (head size)  */
     ATTN_ERR_CUDA = 3,        /* a CUDA runtime/driver call or the kernel launch failed       */
     ATTN_ERR_TIMEOUT = 4      /* a device-side bounded wait ran out (see attn_check_device_status) */
 } attn_status_t;
@@ -45,7 +45,8 @@ typedef enum {
  * k, v device pointers, bf16, [B, Skv, Hkv, D]
  * o    device pointer, bf16, [B, Sq, Hq, D]   (written; round-to-nearest-even of O)
  * lse  device pointer, fp32, [B, Hq, Sq], or NULL to skip it
- * B, Sq, Skv, Hq, Hkv, D  sizes; every one >= 1, Hq a multiple of Hkv, D 64 or 128.
+ * B, Sq, Skv, Hq, Hkv, D  sizes; every one >= 1, Hq a multiple of Hkv, D 64, 128 or 256
+ *      (other head sizes: ATTN_ERR_UNSUPPORTED).
  *      Sq and Skv may be any length (ragged tails are handled in the kernel).
  * causal 0: every key visible.  1: key j visible from query i iff
  *      j <= i + (Skv - Sq) (bottom-right aligned, as in chunked prefill).
@@ -152,7 +153,8 @@ attn_status_t attn_fwd_splitkv_noalloc(const void* q, const void* k, const void*
  * dk, dv    device pointers, [B, Skv, Hkv, D]  (written; every element, zero for
  *           keys no query row sees)
  * B .. scale  as attn_fwd (the same causal mode and scale as the forward call;
- *           the page's backward has no mask, this one applies the forward's).
+ *           the page's backward has no mask, this one applies the forward's);
+ *           D 64 or 128 (D = 256: ATTN_ERR_UNSUPPORTED).
  * dtype     ATTN_DTYPE_BF16 or ATTN_DTYPE_F16: the element type of q, k, v, o,
  *           dO, dq, dk and dv.
  * workspace device pointer, 256-byte aligned, of at least
