@@ -75,7 +75,8 @@ bool opt_in_smem_bwd() {
     return cudaFuncSetAttribute(attn::bwd::fmha_bwd_dkdv_kernel<kF16, kD>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess &&
            cudaFuncSetAttribute(attn::bwd::fmha_bwd_dq_kernel<kF16, kD>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess;
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                attn::bwd::DqGeo<kD>::kSmemBytes) == cudaSuccess;
 }
 
 // Per-device one-time set-up: the kernels' shared-memory opt-in and the SM count.
@@ -543,7 +544,7 @@ attn_status_t launch_bwd(const CUtensorMap* tm, const void* o, const void* dO, c
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);
     const unsigned int g_q = static_cast<unsigned int>(p.B * p.Hq * p.n_q_tiles);
-    fmha_bwd_dq_kernel<kF16, kD><<<g_q, kThreads, BwdGeo<kD>::kSmemBytes, stream>>>(tm[0], tm[1], tm[2], tm[3], p);
+    fmha_bwd_dq_kernel<kF16, kD><<<g_q, kThreads, DqGeo<kD>::kSmemBytes, stream>>>(tm[0], tm[1], tm[2], tm[3], p);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return ATTN_OK;

@@ -559,6 +559,42 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------- dQ
+// Shared memory of the dQ kernel: Q and dO fixed, then separate rings for K
+// (three stages: read by S_n and, at the end of the step, by dQ_n) and V (two
+// stages: read only by dP_n, so a V stage frees early).
+template <int kD>
+struct DqGeo {
+    static_assert(kD == 64 || kD == 128, "head size 64 or 128");
+    static constexpr int kHalves = kD / 64;
+    static constexpr int kTileBytes = kBM * kD * 2;
+    static constexpr int kKStages = 3, kVStages = 2;
+    static constexpr int kFix0 = 0;                                  // Q
+    static constexpr int kFix1 = kTileBytes;                         // dO
+    static constexpr int kKRing = 2 * kTileBytes;
+    static constexpr int kVRing = kKRing + kKStages * kTileBytes;
+    static constexpr int kBar = kVRing + kVStages * kTileBytes;
+    static constexpr int kTmemSlot = kBar + 24 * 8;
+    static constexpr int kAbort = kTmemSlot + 4;
+    static constexpr int kSmemBytes = kAbort + 4 + 1024;
+    static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
+    static constexpr uint32_t kTmemS = 0, kTmemDP = 128, kTmemDQ = 256;
+};
+
+enum : int {
+    DQB_FIXFULL = 0,
+    DQB_KFULL = 1,        // [K stage]
+    DQB_KEMPTY = 4,       // [K stage]
+    DQB_VFULL = 7,        // [V stage]
+    DQB_VEMPTY = 9,       // [V stage]
+    DQB_SFULL = 11,
+    DQB_DPFULL,
+    DQB_PREADY,           // S_n read out of tensor memory (256 arrivals)
+    DQB_DSREADY,          // dS_n in tensor memory (256 arrivals)
+    DQB_ACCDONE,
+    DQB_MMADONE,
+    DQB_COUNT
+};
+static_assert(DQB_COUNT <= 24, "barrier area");
 // Work item of CTA u: (b, hq) = u / n_q_tiles and its query tile t (last tiles
 // first: under a causal mask they visit the most KV tiles); the CTAs of one
 // head stream the same K/V tiles side by side, out of L2.
@@ -567,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fmha_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                        const BwdParams p) {
-    using G = BwdGeo<kD>;
+    using G = DqGeo<kD>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(smem);
@@ -587,17 +623,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const unsigned int limit = p.poll_limit;
 
     if (warp == kLoadWarp && lane == 0) {
-        mbar_init(bar(BAR_FIXFULL), 1);
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(bar(BAR_FULL + s), 1);
-            mbar_init(bar(BAR_EMPTY + s), 1);
+        mbar_init(bar(DQB_FIXFULL), 1);
+        for (int s = 0; s < G::kKStages; ++s) {
+            mbar_init(bar(DQB_KFULL + s), 1);
+            mbar_init(bar(DQB_KEMPTY + s), 1);
         }
-        mbar_init(bar(BAR_SFULL), 1);
-        mbar_init(bar(BAR_DPFULL), 1);
-        mbar_init(bar(BAR_PREADY), 32 * kComputeWarps);
-        mbar_init(bar(BAR_DSREADY), 32 * kComputeWarps);
-        mbar_init(bar(BAR_ACCDONE), 1);
-        mbar_init(bar(BAR_MMADONE), 1);
+        for (int s = 0; s < G::kVStages; ++s) {
+            mbar_init(bar(DQB_VFULL + s), 1);
+            mbar_init(bar(DQB_VEMPTY + s), 1);
+        }
+        mbar_init(bar(DQB_SFULL), 1);
+        mbar_init(bar(DQB_DPFULL), 1);
+        mbar_init(bar(DQB_PREADY), 32 * kComputeWarps);
+        mbar_init(bar(DQB_DSREADY), 32 * kComputeWarps);
+        mbar_init(bar(DQB_ACCDONE), 1);
+        mbar_init(bar(DQB_MMADONE), 1);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tm_q);
@@ -619,30 +659,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0 && nkv > 0) {
             const uint64_t pol_fix = l2_policy_evict_first();
             const uint64_t pol_stream = l2_policy_evict_last();
-            mbar_arrive_expect_tx(bar(BAR_FIXFULL), 2 * G::kTileBytes);
+            mbar_arrive_expect_tx(bar(DQB_FIXFULL), 2 * G::kTileBytes);
             for (int h = 0; h < G::kHalves; ++h) {
-                tma_load_4d(sbase + G::kFix0 + h * kHalfBytes, &tm_q, h * 64, hq, t * kBM, b, bar(BAR_FIXFULL),
+                tma_load_4d(sbase + G::kFix0 + h * kHalfBytes, &tm_q, h * 64, hq, t * kBM, b, bar(DQB_FIXFULL),
                             pol_fix);
-                tma_load_4d(sbase + G::kFix1 + h * kHalfBytes, &tm_do, h * 64, hq, t * kBM, b, bar(BAR_FIXFULL),
+                tma_load_4d(sbase + G::kFix1 + h * kHalfBytes, &tm_do, h * 64, hq, t * kBM, b, bar(DQB_FIXFULL),
                             pol_fix);
             }
-            int issued = 0;
+            int k_issued = 0, v_issued = 0;
             for (int kt = 0; kt < nkv; ++kt) {
-                const int s = kt % kStages, use = kt / kStages;
-                if (use > 0 && !wait_bounded(bar(BAR_EMPTY + s), (use - 1) & 1, abort_flag, limit)) break;
-                mbar_arrive_expect_tx(bar(BAR_FULL + s), 2 * G::kTileBytes);
-                for (int h = 0; h < G::kHalves; ++h) {
-                    tma_load_4d(sbase + G::kRing0 + s * G::kTileBytes + h * kHalfBytes, &tm_k, h * 64, hkv, kt * kBN,
-                                b, bar(BAR_FULL + s), pol_stream);
-                    tma_load_4d(sbase + G::kRing1 + s * G::kTileBytes + h * kHalfBytes, &tm_v, h * 64, hkv, kt * kBN,
-                                b, bar(BAR_FULL + s), pol_stream);
-                }
-                ++issued;
+                const int ks = kt % G::kKStages, kuse = kt / G::kKStages;
+                if (kuse > 0 && !wait_bounded(bar(DQB_KEMPTY + ks), (kuse - 1) & 1, abort_flag, limit)) break;
+                mbar_arrive_expect_tx(bar(DQB_KFULL + ks), G::kTileBytes);
+                for (int h = 0; h < G::kHalves; ++h)
+                    tma_load_4d(sbase + G::kKRing + ks * G::kTileBytes + h * kHalfBytes, &tm_k, h * 64, hkv,
+                                kt * kBN, b, bar(DQB_KFULL + ks), pol_stream);
+                ++k_issued;
+                const int vs = kt % G::kVStages, vuse = kt / G::kVStages;
+                if (vuse > 0 && !wait_bounded(bar(DQB_VEMPTY + vs), (vuse - 1) & 1, abort_flag, limit)) break;
+                mbar_arrive_expect_tx(bar(DQB_VFULL + vs), G::kTileBytes);
+                for (int h = 0; h < G::kHalves; ++h)
+                    tma_load_4d(sbase + G::kVRing + vs * G::kTileBytes + h * kHalfBytes, &tm_v, h * 64, hkv,
+                                kt * kBN, b, bar(DQB_VFULL + vs), pol_stream);
+                ++v_issued;
             }
-            drain_bounded(bar(BAR_FIXFULL), 0, limit);
-            for (int s = 0; s < kStages; ++s) {
-                const int fills = issued > s ? (issued - 1 - s) / kStages + 1 : 0;
-                if (fills) drain_bounded(bar(BAR_FULL + s), (fills - 1) & 1, limit);
+            drain_bounded(bar(DQB_FIXFULL), 0, limit);
+            for (int s = 0; s < G::kKStages; ++s) {
+                const int fills = k_issued > s ? (k_issued - 1 - s) / G::kKStages + 1 : 0;
+                if (fills) drain_bounded(bar(DQB_KFULL + s), (fills - 1) & 1, limit);
+            }
+            for (int s = 0; s < G::kVStages; ++s) {
+                const int fills = v_issued > s ? (v_issued - 1 - s) / G::kVStages + 1 : 0;
+                if (fills) drain_bounded(bar(DQB_VFULL + s), (fills - 1) & 1, limit);
             }
         }
         __syncwarp();
@@ -652,57 +700,61 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint32_t idesc_acc = idesc_f16kind_f32(kBM, kD, true, kF16);  // dQ
         const uint64_t q_desc = sdesc_sw128(sbase + G::kFix0, 16, 1024);
         const uint64_t do_desc = sdesc_sw128(sbase + G::kFix1, 16, 1024);
-        const uint64_t k_k0 = sdesc_sw128(sbase + G::kRing0, 16, 1024);
-        const uint64_t v_k0 = sdesc_sw128(sbase + G::kRing1, 16, 1024);
-        const uint64_t k_mn0 = sdesc_sw128(sbase + G::kRing0, kHalfBytes, 1024);
+        const uint64_t k_k0 = sdesc_sw128(sbase + G::kKRing, 16, 1024);
+        const uint64_t v_k0 = sdesc_sw128(sbase + G::kVRing, 16, 1024);
+        const uint64_t k_mn0 = sdesc_sw128(sbase + G::kKRing, kHalfBytes, 1024);
         const uint32_t tS = tmem_base + G::kTmemS, tDP = tmem_base + G::kTmemDP;
-        const uint32_t tDQ = tmem_base + G::kTmemAcc0;
+        const uint32_t tDQ = tmem_base + G::kTmemDQ;
         // Issue order S_0, dP_0, then per KV tile n:
         //   [S_n read out] S_{n+1}, [dS_n stored] dQ_n, dP_{n+1}
         // The elementwise warps signal (PREADY) as soon as S_n is in their
         // registers, so S_{n+1} runs while they form P_n and dS_n; dP_{n+1}
-        // overwrites dS_n only after dQ_n (issue order).
-        auto issue_s = [&](int kt) -> bool {  // S of KV tile kt; its stage must have landed
-            const int s = kt % kStages;
-            if (!wait_bounded(bar(BAR_FULL + s), (kt / kStages) & 1, abort_flag, limit)) return false;
+        // overwrites dS_n only after dQ_n (issue order).  A V stage is released
+        // right after its dP, a K stage after its dQ.
+        auto issue_s = [&](int kt) -> bool {  // S of KV tile kt; K_kt must have landed
+            const int ks = kt % G::kKStages;
+            if (!wait_bounded(bar(DQB_KFULL + ks), (kt / G::kKStages) & 1, abort_flag, limit)) return false;
             tc_fence_after();
             if (elect_one()) {
-                mma_kmajor<kD>(tS, q_desc, k_k0 + static_cast<uint64_t>((s * G::kTileBytes) >> 4), idesc_s);
-                mma_commit(bar(BAR_SFULL));
+                mma_kmajor<kD>(tS, q_desc, k_k0 + static_cast<uint64_t>((ks * G::kTileBytes) >> 4), idesc_s);
+                mma_commit(bar(DQB_SFULL));
             }
             __syncwarp();
             return true;
         };
-        auto issue_dp = [&](int kt) {
-            const int s = kt % kStages;
+        auto issue_dp = [&](int kt) -> bool {  // dP of KV tile kt; V_kt must have landed
+            const int vs = kt % G::kVStages;
+            if (!wait_bounded(bar(DQB_VFULL + vs), (kt / G::kVStages) & 1, abort_flag, limit)) return false;
+            tc_fence_after();
             if (elect_one()) {
-                mma_kmajor<kD>(tDP, do_desc, v_k0 + static_cast<uint64_t>((s * G::kTileBytes) >> 4), idesc_s);
-                mma_commit(bar(BAR_DPFULL));
+                mma_kmajor<kD>(tDP, do_desc, v_k0 + static_cast<uint64_t>((vs * G::kTileBytes) >> 4), idesc_s);
+                mma_commit(bar(DQB_DPFULL));
+                mma_commit(bar(DQB_VEMPTY + vs));
             }
             __syncwarp();
+            return true;
         };
-        bool ok = nkv > 0 && wait_bounded(bar(BAR_FIXFULL), 0, abort_flag, limit) && issue_s(0);
-        if (ok) issue_dp(0);
+        bool ok = nkv > 0 && wait_bounded(bar(DQB_FIXFULL), 0, abort_flag, limit) && issue_s(0) && issue_dp(0);
         for (int kt = 0; ok && kt < nkv; ++kt) {
-            const int s = kt % kStages;
-            const uint64_t so = static_cast<uint64_t>((s * G::kTileBytes) >> 4);
+            const int ks = kt % G::kKStages;
+            const uint64_t so = static_cast<uint64_t>((ks * G::kTileBytes) >> 4);
             if (kt + 1 < nkv) {
-                if (!wait_bounded(bar(BAR_PREADY), kt & 1, abort_flag, limit)) break;  // S_kt read out
+                if (!wait_bounded(bar(DQB_PREADY), kt & 1, abort_flag, limit)) break;  // S_kt read out
                 if (!issue_s(kt + 1)) break;
             }
-            if (!wait_bounded(bar(BAR_DSREADY), kt & 1, abort_flag, limit)) break;
+            if (!wait_bounded(bar(DQB_DSREADY), kt & 1, abort_flag, limit)) break;
             tc_fence_after();
             if (elect_one()) {
                 mma_tmem_mn(tDQ, tDP, k_mn0 + so, idesc_acc, kt > 0);
-                mma_commit(bar(BAR_EMPTY + s));
-                if (kt == nkv - 1) mma_commit(bar(BAR_ACCDONE));
+                mma_commit(bar(DQB_KEMPTY + ks));
+                if (kt == nkv - 1) mma_commit(bar(DQB_ACCDONE));
             }
             __syncwarp();
-            if (kt + 1 < nkv) issue_dp(kt + 1);
+            if (kt + 1 < nkv && !issue_dp(kt + 1)) break;
         }
         if (elect_one()) {
-            mma_commit(bar(BAR_MMADONE));
-            drain_bounded(bar(BAR_MMADONE), 0, limit);
+            mma_commit(bar(DQB_MMADONE));
+            drain_bounded(bar(DQB_MMADONE), 0, limit);
         }
         __syncwarp();
     } else {
@@ -723,7 +775,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int lim = static_cast<int>(lim_ll < -1 ? -1 : lim_ll);
         bool ok = true;
         for (int kt = 0; kt < nkv; ++kt) {
-            const bool got = wait_bounded(bar(BAR_SFULL), kt & 1, abort_flag, limit);
+            const bool got = wait_bounded(bar(DQB_SFULL), kt & 1, abort_flag, limit);
             if (!__all_sync(0xffffffffu, got)) {
                 ok = false;
                 break;
@@ -732,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t x[64];
             tmem_ld64(tS, x);
             tc_fence_before();
-            mbar_arrive(bar(BAR_PREADY));  // S may now be overwritten by the next tile's product
+            mbar_arrive(bar(DQB_PREADY));  // S may now be overwritten by the next tile's product
             float pv[64];
 #pragma unroll
             for (int c = 0; c < 64; c += 2) {
@@ -746,7 +798,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < 64; ++c)
                     if (c >= nvis) pv[c] = 0.f;
             }
-            const bool got2 = wait_bounded(bar(BAR_DPFULL), kt & 1, abort_flag, limit);
+            const bool got2 = wait_bounded(bar(DQB_DPFULL), kt & 1, abort_flag, limit);
             if (!__all_sync(0xffffffffu, got2)) {
                 ok = false;
                 break;
@@ -766,18 +818,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(BAR_DSREADY));
+            mbar_arrive(bar(DQB_DSREADY));
         }
         bool have = ok && nkv > 0;
         if (have) {
-            const bool got = wait_bounded(bar(BAR_ACCDONE), 0, abort_flag, limit);
+            const bool got = wait_bounded(bar(DQB_ACCDONE), 0, abort_flag, limit);
             have = __all_sync(0xffffffffu, got);
             tc_fence_after();
         }
         if (ok) {
             const bool write = row < p.Sq;
             const size_t off = ((static_cast<size_t>(b) * p.Sq + (write ? row : 0)) * p.Hq + hq) * kD + half * (kD / 2);
-            store_acc_half<kF16, kD>(tmem_base + lane_off + G::kTmemAcc0 + half * (kD / 2), have, p.scale,
+            store_acc_half<kF16, kD>(tmem_base + lane_off + G::kTmemDQ + half * (kD / 2), have, p.scale,
                                      p.dq + off, write);
         }
     }
