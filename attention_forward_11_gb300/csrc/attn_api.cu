@@ -533,9 +533,10 @@ template <bool kF16, int kD>
 attn_status_t launch_bwd(const CUtensorMap* tm, const void* o, const void* dO, const float* lse,
                          const attn::bwd::BwdParams& p, cudaStream_t stream) {
     using namespace attn::bwd;
-    const long long rows = (long long)p.B * p.Hq * p.sq_pad;
+    const long long rows = (long long)p.Hq * p.sq_pad;  // per batch entry
     const long long per_block = 8LL * prep_rows_per_warp<kD>();
-    bwd_prep_kernel<kF16, kD><<<static_cast<unsigned int>((rows + per_block - 1) / per_block), 256, 0, stream>>>(
+    const dim3 prep_grid(static_cast<unsigned int>((rows + per_block - 1) / per_block), static_cast<unsigned int>(p.B));
+    bwd_prep_kernel<kF16, kD><<<prep_grid, 256, 0, stream>>>(
         static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dO), lse, p);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -608,7 +609,7 @@ extern "C" attn_status_t attn_bwd(const void* q, const void* k, const void* v, c
     p.n_kv_tiles = (Skv + attn::kBN - 1) / attn::kBN;
     p.sq_pad = p.n_q_tiles * attn::kBM;
     if ((long long)B * Hkv * p.n_kv_tiles > 0x7fffffffLL || (long long)B * Hq * p.n_q_tiles > 0x7fffffffLL ||
-        ((long long)B * Hq * p.sq_pad + 7) / 8 > 0x7fffffffLL)
+        (long long)Hq * p.sq_pad > 0x7fffffffLL - 1024 || B > 65535)
         return ATTN_ERR_INVALID_ARG;
     p.scale = scale;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);

@@ -163,10 +163,11 @@ __host__ __device__ __forceinline__ int kv_tiles_for_rows(const BwdParams& p, in
 }
 
 // ---------------------------------------------------------------- prep
-// delta and lse2 of every padded row.  Rows are taken in memory order
-// (b, i, h), so a warp's loads of O and dO are contiguous: each lane loads
-// 16 bytes of each, kD / 8 lanes cover a row, and a warp handles kPrepIters
-// groups of 32 / (kD / 8) rows with all loads issued before the reductions.
+// delta and lse2 of every padded row.  Grid: (rows of a batch entry / block,
+// batch).  Within a batch entry rows are taken in memory order (i, h), so a
+// warp's loads of O and dO are contiguous: each lane loads 16 bytes of each,
+// kD / 8 lanes cover a row, and a warp handles kPrepIters groups of
+// 32 / (kD / 8) rows with all loads issued before the reductions.
 constexpr int kPrepIters = 4;
 template <int kD>
 __host__ __device__ constexpr int prep_rows_per_warp() {
@@ -180,22 +181,19 @@ __global__ void __launch_bounds__(256)
     constexpr int kL = kD / 8;          // lanes per row
     constexpr int kR = 32 / kL;         // rows per load instruction
     const int lane = static_cast<int>(threadIdx.x) & 31;
-    const long long total = (long long)p.B * p.sq_pad * p.Hq;
-    const long long row0 = ((long long)blockIdx.x * 8 + threadIdx.x / 32) * (kR * kPrepIters);
+    const int b = static_cast<int>(blockIdx.y);
+    const int per_batch = p.sq_pad * p.Hq;  // rows (i, h) of one batch entry, in memory order
+    const int row0 = (static_cast<int>(blockIdx.x) * 8 + static_cast<int>(threadIdx.x) / 32) * (kR * kPrepIters);
     uint4 ov[kPrepIters], dv[kPrepIters];
-    long long rr[kPrepIters];
-    bool live[kPrepIters];
+    int ii[kPrepIters], hh[kPrepIters];
 #pragma unroll
     for (int it = 0; it < kPrepIters; ++it) {
-        const long long r = row0 + it * kR + lane / kL;  // (b, i, h) in memory order over padded rows
-        rr[it] = r;
-        const int i = r < total ? static_cast<int>((r / p.Hq) % p.sq_pad) : p.Sq;
-        live[it] = i < p.Sq;
+        const int r = row0 + it * kR + lane / kL;
+        ii[it] = r < per_batch ? r / p.Hq : p.sq_pad;
+        hh[it] = r - (r / p.Hq) * p.Hq;
         ov[it] = dv[it] = make_uint4(0u, 0u, 0u, 0u);
-        if (live[it]) {
-            const long long b = r / ((long long)p.sq_pad * p.Hq);
-            const int h = static_cast<int>(r % p.Hq);
-            const size_t off = ((static_cast<size_t>(b) * p.Sq + i) * p.Hq + h) * kD + 8 * (lane % kL);
+        if (ii[it] < p.Sq) {
+            const size_t off = ((static_cast<size_t>(b) * p.Sq + ii[it]) * p.Hq + hh[it]) * kD + 8 * (lane % kL);
             ov[it] = *reinterpret_cast<const uint4*>(o + off);
             dv[it] = *reinterpret_cast<const uint4*>(dO + off);
         }
@@ -212,14 +210,11 @@ __global__ void __launch_bounds__(256)
         }
 #pragma unroll
         for (int sft = kL / 2; sft > 0; sft >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sft);
-        const long long r = rr[it];
-        if (lane % kL == 0 && r < total) {
-            const long long b = r / ((long long)p.sq_pad * p.Hq);
-            const int i = static_cast<int>((r / p.Hq) % p.sq_pad);
-            const int h = static_cast<int>(r % p.Hq);
+        const int i = ii[it], h = hh[it];
+        if (lane % kL == 0 && i < p.sq_pad) {
             const size_t w = (static_cast<size_t>(b) * p.Hq + h) * p.sq_pad + i;
             float l2 = INFINITY, dl = 0.f;
-            if (live[it]) {
+            if (i < p.Sq) {
                 const float l = lse[(static_cast<size_t>(b) * p.Hq + h) * p.Sq + i];
                 l2 = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
                 dl = acc;
