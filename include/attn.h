@@ -154,7 +154,7 @@ attn_status_t attn_fwd_splitkv_noalloc(const void* q, const void* k, const void*
  *           keys no query row sees)
  * B .. scale  as attn_fwd (the same causal mode and scale as the forward call;
  *           the page's backward has no mask, this one applies the forward's);
- *           D 64 or 128 (D = 256: ATTN_ERR_UNSUPPORTED).
+ *           D 64 or 128 (D = 256: ATTN_ERR_UNSUPPORTED); B <= 65535.
  * dtype     ATTN_DTYPE_BF16 or ATTN_DTYPE_F16: the element type of q, k, v, o,
  *           dO, dq, dk and dv.
  * workspace device pointer, 256-byte aligned, of at least
