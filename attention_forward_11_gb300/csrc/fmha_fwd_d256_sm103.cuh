@@ -64,7 +64,9 @@ struct Geo {
 
 constexpr uint32_t kTmemO = 256;
 
-// Work item of CTA u: query tile (b, hq, t); tiles that visit the most KV tiles
+// Work item of CTA u: query tile t of (b, hq) = u / n_t.  The CTAs of one head
+// run side by side, so its K and V (4 MB at S = 4096) stay in L2 while they
+// stream through them; within a head the tiles that visit the most KV tiles
 // (the last ones under a causal mask) go first.
 struct Item {
     int b, hq, hkv, row0, n;
@@ -73,8 +75,8 @@ struct Item {
 __host__ __device__ __forceinline__ Item decode(const FwdParams& p, int u) {
     Item it;
     const int n_t = (p.Sq + kBM - 1) / kBM;
-    const int bh = u % (p.B * p.Hq);
-    const int tr = u / (p.B * p.Hq);
+    const int bh = u / n_t;
+    const int tr = u % n_t;
     const int t = p.causal ? n_t - 1 - tr : tr;
     it.b = bh / p.Hq;
     it.hq = bh % p.Hq;
