@@ -531,7 +531,7 @@ size_t bwd_vec_bytes(int B, int Sq, int Hq) {
 
 template <bool kF16, int kD>
 attn_status_t launch_bwd(const CUtensorMap* tm, const void* o, const void* dO, const float* lse,
-                         const attn::bwd::BwdParams& p, cudaStream_t stream) {
+                         const attn::bwd::BwdParams& p, int sms, cudaStream_t stream) {
     using namespace attn::bwd;
     const long long rows = (long long)p.Hq * p.sq_pad;  // per batch entry
     const long long per_block = 8LL * prep_rows_per_warp<kD>();
@@ -540,7 +540,9 @@ attn_status_t launch_bwd(const CUtensorMap* tm, const void* o, const void* dO, c
         static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dO), lse, p);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);
-    const unsigned int g_kv = static_cast<unsigned int>(p.B * p.Hkv * p.n_kv_tiles);
+    // persistent: at most one CTA per SM, items taken from the queue the prep kernel reset
+    const int n_items = p.B * p.Hkv * p.n_kv_tiles;
+    const unsigned int g_kv = static_cast<unsigned int>(n_items < sms ? n_items : sms);
     fmha_bwd_dkdv_kernel<kF16, kD><<<g_kv, kThreads, BwdGeo<kD>::kSmemBytes, stream>>>(tm[0], tm[1], tm[2], tm[3], p);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -559,7 +561,7 @@ extern "C" attn_status_t attn_bwd_workspace_size(int B, int Sq, int Skv, int Hq,
     const attn_status_t st = check_sizes(B, Sq, Skv, Hq, Hkv, D, 0);
     if (st != ATTN_OK) return st;
     if (D == 256) return ATTN_ERR_UNSUPPORTED;  // the backward kernels take D <= 128
-    *bytes = 2 * bwd_vec_bytes(B, Sq, Hq);
+    *bytes = 2 * bwd_vec_bytes(B, Sq, Hq) + kBwdAlign;  // + the dK/dV kernel's work counter
     return ATTN_OK;
 }
 
@@ -582,7 +584,7 @@ extern "C" attn_status_t attn_bwd(const void* q, const void* k, const void* v, c
     const int Dn = D > 0 ? D : 1;
     const size_t q_bytes = (size_t)B * Sq * Hq * Dn * 2, kv_bytes = (size_t)B * Skv * Hkv * Dn * 2;
     const size_t lse_bytes = (size_t)B * Hq * Sq * 4;
-    const size_t need = 2 * bwd_vec_bytes(B, Sq, Hq);
+    const size_t need = 2 * bwd_vec_bytes(B, Sq, Hq) + kBwdAlign;
     if (workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
     // the outputs and the workspace overlap no input and no other output
     const void* out_p[4] = {dq, dk, dv, workspace};
@@ -615,6 +617,7 @@ extern "C" attn_status_t attn_bwd(const void* q, const void* k, const void* v, c
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     p.lse2 = static_cast<float*>(workspace);
     p.delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + bwd_vec_bytes(B, Sq, Hq));
+    p.work = reinterpret_cast<int*>(static_cast<char*>(workspace) + 2 * bwd_vec_bytes(B, Sq, Hq));
     p.dq = static_cast<uint16_t*>(dq);
     p.dk = static_cast<uint16_t*>(dk);
     p.dv = static_cast<uint16_t*>(dv);
@@ -627,8 +630,10 @@ extern "C" attn_status_t attn_bwd(const void* q, const void* k, const void* v, c
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || !device_setup(dev, &sms)) return ATTN_ERR_CUDA;
     if (D == 64)
-        return f16 ? launch_bwd<true, 64>(tm, o, dO, lse, p, stream) : launch_bwd<false, 64>(tm, o, dO, lse, p, stream);
-    return f16 ? launch_bwd<true, 128>(tm, o, dO, lse, p, stream) : launch_bwd<false, 128>(tm, o, dO, lse, p, stream);
+        return f16 ? launch_bwd<true, 64>(tm, o, dO, lse, p, sms, stream)
+                   : launch_bwd<false, 64>(tm, o, dO, lse, p, sms, stream);
+    return f16 ? launch_bwd<true, 128>(tm, o, dO, lse, p, sms, stream)
+               : launch_bwd<false, 128>(tm, o, dO, lse, p, sms, stream);
 }
 
 extern "C" const char* attn_status_str(attn_status_t status) {

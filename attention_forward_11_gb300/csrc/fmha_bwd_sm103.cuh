@@ -46,16 +46,22 @@ constexpr int kThreads = 320;
 constexpr int kStages = 2;
 constexpr int kVecBytes = kBM * 4;  // lse2 or delta of one 128-row tile
 
+// Barriers of the dK/dV kernel.
 enum : int {
-    BAR_FIXFULL = 0,
-    BAR_FULL = 1,                  // [stage]
+    BAR_KFULL = 0,                 // the item's K tile landed
+    BAR_KEMPTY,                    // its last S^T completed: K may be replaced
+    BAR_VFULL,
+    BAR_VEMPTY,                    // its last dP^T completed: V may be replaced
+    BAR_FULL,                      // [stage] Q, dO and their lse2 / delta
     BAR_EMPTY = BAR_FULL + kStages,
     BAR_SFULL = BAR_EMPTY + kStages,
     BAR_DPFULL,
-    BAR_PREADY,                    // dK/dV: P^T in tensor memory; dQ: S read out (256 arrivals)
-    BAR_DSREADY,                   // dS (or dS^T) in tensor memory (256 arrivals)
-    BAR_ACCDONE,                   // every accumulating MMA completed
-    BAR_MMADONE,                   // teardown
+    BAR_PREADY,                    // P^T in tensor memory (256 arrivals)
+    BAR_DSREADY,                   // dS^T in tensor memory (256 arrivals)
+    BAR_ACCDONE,                   // the item's last dK completed
+    BAR_ITEMFULL,                  // [2] next work item published
+    BAR_ITEMEMPTY = BAR_ITEMFULL + 2,  // [2] read by the MMA warp and the 8 elementwise warps
+    BAR_MMADONE = BAR_ITEMEMPTY + 2,   // teardown
     BAR_COUNT
 };
 
@@ -74,7 +80,8 @@ struct BwdGeo {
     static constexpr int kBar = kVec + kStages * 2 * kVecBytes;
     static constexpr int kTmemSlot = kBar + BAR_COUNT * 8;
     static constexpr int kAbort = kTmemSlot + 4;
-    static constexpr int kSmemBytes = kAbort + 4 + 1024;
+    static constexpr int kItems = kAbort + 4;          // [2] published work items
+    static constexpr int kSmemBytes = kItems + 8 + 1024;
     static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
     // tensor-memory columns
     static constexpr uint32_t kTmemS = 0;
@@ -95,6 +102,7 @@ struct BwdParams {
     uint16_t* dq;               // [B, Sq, Hq, D]
     uint16_t* dk;               // [B, Skv, Hkv, D]
     uint16_t* dv;               // [B, Skv, Hkv, D]
+    int* work;                  // work-item counter of the dK/dV kernel (zeroed by prep)
     int n_q_tiles, n_kv_tiles;
     unsigned int poll_limit;
 };
@@ -182,6 +190,7 @@ __global__ void __launch_bounds__(256)
     constexpr int kR = 32 / kL;         // rows per load instruction
     const int lane = static_cast<int>(threadIdx.x) & 31;
     const int b = static_cast<int>(blockIdx.y);
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.work = 0;  // the dK/dV kernel's queue
     const int per_batch = p.sq_pad * p.Hq;  // rows (i, h) of one batch entry, in memory order
     const int row0 = (static_cast<int>(blockIdx.x) * 8 + static_cast<int>(threadIdx.x) / 32) * (kR * kPrepIters);
     uint4 ov[kPrepIters], dv[kPrepIters];
@@ -293,12 +302,32 @@ __device__ __forceinline__ void store_acc_half(uint32_t taddr, bool have, float 
 }
 
 // ---------------------------------------------------------------- dK / dV
-// Work item of CTA u: (b, hkv) = u / n_kv_tiles, KV tile n = u % n_kv_tiles.
-// The CTAs of one head run side by side, so the Q and dO tiles they all stream
-// stay in L2 (a few heads' worth at a time instead of every head's); within a
-// head the tiles near the start of the keys, which see the most query rows
-// under a causal mask, go first.
-// tm_a / tm_b: Q and dO (streamed); tm_k / tm_v: K and V (fixed).
+// Work item u = one (b, hkv, 128-key tile).  Items are numbered in blocks of
+// kItemHeads heads: within a block by KV tile (the tiles near the start of the
+// keys, which see the most query rows under a causal mask, first), then by
+// head.  So the longest items come first within each block, and the CTAs in
+// flight work on a few heads at a time, whose Q and dO stay in L2.
+constexpr int kItemHeads = 4;
+
+__host__ __device__ __forceinline__ void dkdv_item(const BwdParams& p, int u, int& b, int& hkv, int& n) {
+    const int nbh = p.B * p.Hkv;
+    const int per_block = kItemHeads * p.n_kv_tiles;
+    const int blk = u / per_block;
+    const int within = u - blk * per_block;
+    const int heads = nbh - blk * kItemHeads < kItemHeads ? nbh - blk * kItemHeads : kItemHeads;
+    n = within / heads;
+    const int bh = blk * kItemHeads + (within - n * heads);
+    b = bh / p.Hkv;
+    hkv = bh % p.Hkv;
+}
+
+// Persistent: at most one CTA per SM; the TMA warp takes items from a global
+// counter (the prep kernel zeroes it) and publishes each through a two-slot
+// ring in shared memory.  The Q/dO ring and the per-step barriers run on across
+// items; K of the next item is loaded as soon as the current item's last S^T
+// has read its K, V as soon as its last dP^T has read its V, and the next
+// item's first dV / dK (which start the accumulators afresh) come only after
+// the elementwise warps have read the current accumulators out.
 template <bool kF16, int kD>
 __global__ void __launch_bounds__(kThreads, 1)
     fmha_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -311,22 +340,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) / 32, 0);
     const int lane = static_cast<int>(threadIdx.x) & 31;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + G::kAbort);
+    volatile int* item_slot = reinterpret_cast<volatile int*>(smem + G::kItems);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::kTmemSlot);
     auto bar = [&](int i) -> uint32_t { return sbase + G::kBar + 8 * i; };
-
-    const int u = static_cast<int>(blockIdx.x);
-    const int bh = u / p.n_kv_tiles;
-    const int n = u % p.n_kv_tiles;
-    const int b = bh / p.Hkv, hkv = bh % p.Hkv;
+    const int n_items = p.B * p.Hkv * p.n_kv_tiles;
     const int group = p.Hq / p.Hkv;
-    const int r0 = first_row_for_kv_tile(p, n);
-    const int t0 = r0 >= p.Sq ? p.n_q_tiles : r0 / kBM;  // no query row sees the tile: no steps
-    const int tiles_per_head = p.n_q_tiles - t0;  // >= 0
-    const int steps = group * tiles_per_head;     // (head, query tile) pairs
     const unsigned int limit = p.poll_limit;
+    // the item's first query tile and number of (head, query tile) steps
+    auto steps_of = [&](int n, int& t0, int& tiles_per_head) {
+        const int r0 = first_row_for_kv_tile(p, n);
+        t0 = r0 >= p.Sq ? p.n_q_tiles : r0 / kBM;  // no query row sees the tile: no steps
+        tiles_per_head = p.n_q_tiles - t0;
+        return group * tiles_per_head;
+    };
 
     if (warp == kLoadWarp && lane == 0) {
-        mbar_init(bar(BAR_FIXFULL), 1);
+        mbar_init(bar(BAR_KFULL), 1);
+        mbar_init(bar(BAR_KEMPTY), 1);
+        mbar_init(bar(BAR_VFULL), 1);
+        mbar_init(bar(BAR_VEMPTY), 1);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar(BAR_FULL + s), 1);
             mbar_init(bar(BAR_EMPTY + s), 1);
@@ -336,6 +368,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(BAR_PREADY), 32 * kComputeWarps);
         mbar_init(bar(BAR_DSREADY), 32 * kComputeWarps);
         mbar_init(bar(BAR_ACCDONE), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(BAR_ITEMFULL + i), 1);
+            mbar_init(bar(BAR_ITEMEMPTY + i), 1 + kComputeWarps);
+        }
         mbar_init(bar(BAR_MMADONE), 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -355,38 +391,65 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == kLoadWarp) {
         // =========================== TMA producer ===========================
-        if (lane == 0 && steps > 0) {
+        if (lane == 0) {
             const uint64_t pol_fix = l2_policy_evict_first();
             const uint64_t pol_stream = l2_policy_evict_last();
-            mbar_arrive_expect_tx(bar(BAR_FIXFULL), 2 * G::kTileBytes);
-            for (int h = 0; h < G::kHalves; ++h) {
-                tma_load_4d(sbase + G::kFix0 + h * kHalfBytes, &tm_k, h * 64, hkv, n * kBN, b, bar(BAR_FIXFULL),
-                            pol_fix);
-                tma_load_4d(sbase + G::kFix1 + h * kHalfBytes, &tm_v, h * 64, hkv, n * kBN, b, bar(BAR_FIXFULL),
-                            pol_fix);
-            }
-            int issued = 0;
-            for (int st = 0; st < steps; ++st) {
-                const int s = st % kStages, use = st / kStages;
-                if (use > 0 && !wait_bounded(bar(BAR_EMPTY + s), (use - 1) & 1, abort_flag, limit)) break;
-                const int hq = hkv * group + st / tiles_per_head;
-                const int t = t0 + st % tiles_per_head;
-                mbar_arrive_expect_tx(bar(BAR_FULL + s), 2 * G::kTileBytes + 2 * kVecBytes);
-                for (int h = 0; h < G::kHalves; ++h) {
-                    tma_load_4d(sbase + G::kRing0 + s * G::kTileBytes + h * kHalfBytes, &tm_q, h * 64, hq, t * kBM,
-                                b, bar(BAR_FULL + s), pol_stream);
-                    tma_load_4d(sbase + G::kRing1 + s * G::kTileBytes + h * kHalfBytes, &tm_do, h * 64, hq,
-                                t * kBM, b, bar(BAR_FULL + s), pol_stream);
+            int g = 0, w = 0;  // ring fills issued, items with work loaded
+            for (int j = 0;; ++j) {
+                // take the next item and publish it
+                const int slot = j & 1;
+                if (j >= 2 && !wait_bounded(bar(BAR_ITEMEMPTY + slot), ((j >> 1) - 1) & 1, abort_flag, limit)) break;
+                int u = *abort_flag ? -1 : atomicAdd(p.work, 1);
+                if (u >= n_items) u = -1;
+                item_slot[slot] = u;
+                mbar_arrive(bar(BAR_ITEMFULL + slot));
+                if (u < 0) break;
+                int b, hkv, n, t0, tiles_per_head;
+                dkdv_item(p, u, b, hkv, n);
+                const int steps = steps_of(n, t0, tiles_per_head);
+                if (steps == 0) continue;
+                // K, then V of this item, each once the previous item no longer reads it
+                if (w > 0 && !wait_bounded(bar(BAR_KEMPTY), (w - 1) & 1, abort_flag, limit)) break;
+                mbar_arrive_expect_tx(bar(BAR_KFULL), G::kTileBytes);
+                for (int h = 0; h < G::kHalves; ++h)
+                    tma_load_4d(sbase + G::kFix0 + h * kHalfBytes, &tm_k, h * 64, hkv, n * kBN, b, bar(BAR_KFULL),
+                                pol_fix);
+                if (w > 0 && !wait_bounded(bar(BAR_VEMPTY), (w - 1) & 1, abort_flag, limit)) break;
+                mbar_arrive_expect_tx(bar(BAR_VFULL), G::kTileBytes);
+                for (int h = 0; h < G::kHalves; ++h)
+                    tma_load_4d(sbase + G::kFix1 + h * kHalfBytes, &tm_v, h * 64, hkv, n * kBN, b, bar(BAR_VFULL),
+                                pol_fix);
+                ++w;
+                bool ok = true;
+                for (int st = 0; st < steps; ++st, ++g) {
+                    const int s = g % kStages, use = g / kStages;
+                    if (use > 0 && !wait_bounded(bar(BAR_EMPTY + s), (use - 1) & 1, abort_flag, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    const int hq = hkv * group + st / tiles_per_head;
+                    const int t = t0 + st % tiles_per_head;
+                    mbar_arrive_expect_tx(bar(BAR_FULL + s), 2 * G::kTileBytes + 2 * kVecBytes);
+                    for (int h = 0; h < G::kHalves; ++h) {
+                        tma_load_4d(sbase + G::kRing0 + s * G::kTileBytes + h * kHalfBytes, &tm_q, h * 64, hq,
+                                    t * kBM, b, bar(BAR_FULL + s), pol_stream);
+                        tma_load_4d(sbase + G::kRing1 + s * G::kTileBytes + h * kHalfBytes, &tm_do, h * 64, hq,
+                                    t * kBM, b, bar(BAR_FULL + s), pol_stream);
+                    }
+                    const size_t vo = (static_cast<size_t>(b) * p.Hq + hq) * p.sq_pad + static_cast<size_t>(t) * kBM;
+                    bulk_load(sbase + G::kVec + s * 2 * kVecBytes, p.lse2 + vo, kVecBytes, bar(BAR_FULL + s));
+                    bulk_load(sbase + G::kVec + s * 2 * kVecBytes + kVecBytes, p.delta + vo, kVecBytes,
+                              bar(BAR_FULL + s));
                 }
-                const size_t vo = (static_cast<size_t>(b) * p.Hq + hq) * p.sq_pad + static_cast<size_t>(t) * kBM;
-                bulk_load(sbase + G::kVec + s * 2 * kVecBytes, p.lse2 + vo, kVecBytes, bar(BAR_FULL + s));
-                bulk_load(sbase + G::kVec + s * 2 * kVecBytes + kVecBytes, p.delta + vo, kVecBytes,
-                          bar(BAR_FULL + s));
-                ++issued;
+                if (!ok) break;
             }
-            drain_bounded(bar(BAR_FIXFULL), 0, limit);
+            // drain: every copy issued has landed before the CTA may exit
+            if (w > 0) {
+                drain_bounded(bar(BAR_KFULL), (w - 1) & 1, limit);
+                drain_bounded(bar(BAR_VFULL), (w - 1) & 1, limit);
+            }
             for (int s = 0; s < kStages; ++s) {
-                const int fills = issued > s ? (issued - 1 - s) / kStages + 1 : 0;
+                const int fills = g > s ? (g - 1 - s) / kStages + 1 : 0;
                 if (fills) drain_bounded(bar(BAR_FULL + s), (fills - 1) & 1, limit);
             }
         }
@@ -403,50 +466,90 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t do_mn0 = sdesc_sw128(sbase + G::kRing1, kHalfBytes, 1024);
         const uint32_t tS = tmem_base + G::kTmemS, tDP = tmem_base + G::kTmemDP;
         const uint32_t tDV = tmem_base + G::kTmemAcc0, tDK = tmem_base + G::kTmemAcc1;
-        // Issue order S^T_0, dP^T_0, then per step t:
+        // Per item, issue order S^T_0, dP^T_0, then per step t:
         //   dV_t, S^T_{t+1}, dK_t, dP^T_{t+1}
         // so each elementwise phase (P^T_t before dV_t, dS^T_t before dK_t) is
         // covered by two products.  S^T_{t+1} overwrites P^T_t after dV_t has read
         // it and dP^T_{t+1} overwrites dS^T_t after dK_t (one thread's tcgen05
-        // MMAs execute in issue order).
-        auto issue_s = [&](int st) -> bool {  // S^T of step st; its stage must have landed
-            const int s = st % kStages;
-            if (!wait_bounded(bar(BAR_FULL + s), (st / kStages) & 1, abort_flag, limit)) return false;
+        // MMAs execute in issue order).  g counts steps over all items.
+        auto stage_off = [](int gs) { return static_cast<uint64_t>(((gs % kStages) * G::kTileBytes) >> 4); };
+        auto issue_s = [&](int gs) -> bool {  // S^T of global step gs; its stage must have landed
+            if (!wait_bounded(bar(BAR_FULL + gs % kStages), (gs / kStages) & 1, abort_flag, limit)) return false;
             tc_fence_after();
             if (elect_one()) {
-                mma_kmajor<kD>(tS, k_desc, q_k0 + static_cast<uint64_t>((s * G::kTileBytes) >> 4), idesc_s);
+                mma_kmajor<kD>(tS, k_desc, q_k0 + stage_off(gs), idesc_s);
                 mma_commit(bar(BAR_SFULL));
             }
             __syncwarp();
             return true;
         };
-        auto issue_dp = [&](int st) {
-            const int s = st % kStages;
+        auto issue_dp = [&](int gs) {
             if (elect_one()) {
-                mma_kmajor<kD>(tDP, v_desc, do_k0 + static_cast<uint64_t>((s * G::kTileBytes) >> 4), idesc_s);
+                mma_kmajor<kD>(tDP, v_desc, do_k0 + stage_off(gs), idesc_s);
                 mma_commit(bar(BAR_DPFULL));
             }
             __syncwarp();
         };
-        bool ok = steps > 0 && wait_bounded(bar(BAR_FIXFULL), 0, abort_flag, limit) && issue_s(0);
-        if (ok) issue_dp(0);
-        for (int st = 0; ok && st < steps; ++st) {
-            const int s = st % kStages;
-            const uint64_t so = static_cast<uint64_t>((s * G::kTileBytes) >> 4);
-            if (!wait_bounded(bar(BAR_PREADY), st & 1, abort_flag, limit)) break;
-            tc_fence_after();
-            if (elect_one()) mma_tmem_mn(tDV, tS, do_mn0 + so, idesc_acc, st > 0);
+        auto commit_to = [&](int which) {
+            if (elect_one()) mma_commit(bar(which));
             __syncwarp();
-            if (st + 1 < steps && !issue_s(st + 1)) break;
-            if (!wait_bounded(bar(BAR_DSREADY), st & 1, abort_flag, limit)) break;
+        };
+        bool ok = true;
+        int g = 0, w = 0;
+        for (int j = 0; ok; ++j) {
+            const int slot = j & 1;
+            if (!wait_bounded(bar(BAR_ITEMFULL + slot), (j >> 1) & 1, abort_flag, limit)) break;
+            const int u = item_slot[slot];
+            __syncwarp();
+            if (elect_one()) mbar_arrive(bar(BAR_ITEMEMPTY + slot));
+            __syncwarp();
+            if (u < 0) break;
+            int b, hkv, n, t0, tiles_per_head;
+            dkdv_item(p, u, b, hkv, n);
+            const int steps = steps_of(n, t0, tiles_per_head);
+            if (steps == 0) continue;
+            ok = wait_bounded(bar(BAR_KFULL), w & 1, abort_flag, limit) && issue_s(g);
+            if (!ok) break;
+            if (steps == 1) commit_to(BAR_KEMPTY);  // the item's only S^T is issued
+            ok = wait_bounded(bar(BAR_VFULL), w & 1, abort_flag, limit);
+            if (!ok) break;
             tc_fence_after();
-            if (elect_one()) {
-                mma_tmem_mn(tDK, tDP, q_mn0 + so, idesc_acc, st > 0);
-                mma_commit(bar(BAR_EMPTY + s));
-                if (st == steps - 1) mma_commit(bar(BAR_ACCDONE));
+            issue_dp(g);
+            if (steps == 1) commit_to(BAR_VEMPTY);
+            for (int st = 0; ok && st < steps; ++st) {
+                const int gs = g + st;
+                if (!wait_bounded(bar(BAR_PREADY), gs & 1, abort_flag, limit)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (elect_one()) mma_tmem_mn(tDV, tS, do_mn0 + stage_off(gs), idesc_acc, st > 0);
+                __syncwarp();
+                if (st + 1 < steps) {
+                    if (!issue_s(gs + 1)) {
+                        ok = false;
+                        break;
+                    }
+                    if (st + 2 == steps) commit_to(BAR_KEMPTY);  // the item's last S^T is issued
+                }
+                if (!wait_bounded(bar(BAR_DSREADY), gs & 1, abort_flag, limit)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (elect_one()) {
+                    mma_tmem_mn(tDK, tDP, q_mn0 + stage_off(gs), idesc_acc, st > 0);
+                    mma_commit(bar(BAR_EMPTY + gs % kStages));
+                    if (st == steps - 1) mma_commit(bar(BAR_ACCDONE));
+                }
+                __syncwarp();
+                if (st + 1 < steps) {
+                    issue_dp(gs + 1);
+                    if (st + 2 == steps) commit_to(BAR_VEMPTY);  // the item's last dP^T is issued
+                }
             }
-            __syncwarp();
-            if (st + 1 < steps) issue_dp(st + 1);
+            g += steps;
+            ++w;
         }
         if (elect_one()) {
             mma_commit(bar(BAR_MMADONE));
@@ -457,7 +560,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // =========================== elementwise warps ======================
         const int quarter = warp % 4, half = warp / 4;
         const int jr = quarter * 32 + lane;  // key within the tile = TMEM lane
-        const int key = n * kBN + jr;
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t tS = tmem_base + lane_off + G::kTmemS + 64 * half;
         const uint32_t tP = tmem_base + lane_off + G::kTmemS + 64 * half;  // packed over own fp32 columns
@@ -465,83 +567,105 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tDS = tmem_base + lane_off + G::kTmemDP + 64 * half;  // packed over own fp32 columns
         const float sl2 = p.scale_log2;
         bool ok = true;
-        for (int st = 0; st < steps; ++st) {
-            const int s = st % kStages, use = st / kStages;
-            const int t = t0 + st % tiles_per_head;
-            // the stage's lse2 / delta have landed (visible to this thread), and S^T is in TMEM
-            const bool got = wait_bounded(bar(BAR_FULL + s), use & 1, abort_flag, limit) &&
-                             wait_bounded(bar(BAR_SFULL), st & 1, abort_flag, limit);
-            if (!__all_sync(0xffffffffu, got)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const float* l2 = reinterpret_cast<const float*>(smem + G::kVec + s * 2 * kVecBytes) + 64 * half;
-            const float* dl = l2 + kBM;
-            uint32_t x[64];
-            tmem_ld64(tS, x);
-            // row i = t*128 + 64*half + c sees this key iff key <= i + diag
-            const int row0 = t * kBM + 64 * half;
-            const int cmin = p.causal ? key - p.diag - row0 : -1;  // first visible column
-            float pv[64];
-#pragma unroll
-            for (int c = 0; c < 64; c += 2) {
-                ffma2_b(pv[c], pv[c + 1], __uint_as_float(x[c]), __uint_as_float(x[c + 1]), sl2, -l2[c], -l2[c + 1]);
-                pv[c] = ex2_approx(pv[c]);
-                pv[c + 1] = ex2_approx(pv[c + 1]);
-            }
-            if (cmin > 0) {
-#pragma unroll
-                for (int c = 0; c < 64; ++c)
-                    if (c < cmin) pv[c] = 0.f;
-            }
-            {
-                uint32_t pk[32];
-#pragma unroll
-                for (int c = 0; c < 32; ++c) pk[c] = pack_x2<kF16>(pv[2 * c], pv[2 * c + 1]);
-                tmem_st16(tP, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-                tmem_st16(tP + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(bar(BAR_PREADY));
-            const bool got2 = wait_bounded(bar(BAR_DPFULL), st & 1, abort_flag, limit);
-            if (!__all_sync(0xffffffffu, got2)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            tmem_ld64(tDP, x);
-            {
-                uint32_t pk[32];
+        int g = 0, w = 0;
+        for (int j = 0; ok; ++j) {
+            const int slot = j & 1;
+            const bool got_item = wait_bounded(bar(BAR_ITEMFULL + slot), (j >> 1) & 1, abort_flag, limit);
+            if (!__all_sync(0xffffffffu, got_item)) break;
+            const int u = item_slot[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(BAR_ITEMEMPTY + slot));
+            if (u < 0) break;
+            int b, hkv, n, t0, tiles_per_head;
+            dkdv_item(p, u, b, hkv, n);
+            const int steps = steps_of(n, t0, tiles_per_head);
+            const int key = n * kBN + jr;
+            for (int st = 0; st < steps; ++st) {
+                const int gs = g + st;
+                const int s = gs % kStages, use = gs / kStages;
+                const int t = t0 + st % tiles_per_head;
+                // the stage's lse2 / delta have landed (visible to this thread), and S^T is in TMEM
+                const bool got = wait_bounded(bar(BAR_FULL + s), use & 1, abort_flag, limit) &&
+                                 wait_bounded(bar(BAR_SFULL), gs & 1, abort_flag, limit);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const float* l2 = reinterpret_cast<const float*>(smem + G::kVec + s * 2 * kVecBytes) + 64 * half;
+                const float* dl = l2 + kBM;
+                uint32_t x[64];
+                tmem_ld64(tS, x);
+                // row i = t*128 + 64*half + c sees this key iff key <= i + diag
+                const int row0 = t * kBM + 64 * half;
+                const int cmin = p.causal ? key - p.diag - row0 : -1;  // first visible column
+                float pv[64];
 #pragma unroll
                 for (int c = 0; c < 64; c += 2) {
-                    float d0, d1;
-                    fsubmul2(d0, d1, pv[c], pv[c + 1], __uint_as_float(x[c]), __uint_as_float(x[c + 1]), dl[c],
-                             dl[c + 1]);
-                    pk[c / 2] = pack_x2<kF16>(d0, d1);
+                    ffma2_b(pv[c], pv[c + 1], __uint_as_float(x[c]), __uint_as_float(x[c + 1]), sl2, -l2[c],
+                            -l2[c + 1]);
+                    pv[c] = ex2_approx(pv[c]);
+                    pv[c + 1] = ex2_approx(pv[c + 1]);
                 }
-                tmem_st16(tDS, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-                tmem_st16(tDS + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+                if (cmin > 0) {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c)
+                        if (c < cmin) pv[c] = 0.f;
+                }
+                {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) pk[c] = pack_x2<kF16>(pv[2 * c], pv[2 * c + 1]);
+                    tmem_st16(tP, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+                    tmem_st16(tP + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar(BAR_PREADY));
+                const bool got2 = wait_bounded(bar(BAR_DPFULL), gs & 1, abort_flag, limit);
+                if (!__all_sync(0xffffffffu, got2)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                tmem_ld64(tDP, x);
+                {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int c = 0; c < 64; c += 2) {
+                        float d0, d1;
+                        fsubmul2(d0, d1, pv[c], pv[c + 1], __uint_as_float(x[c]), __uint_as_float(x[c + 1]), dl[c],
+                                 dl[c + 1]);
+                        pk[c / 2] = pack_x2<kF16>(d0, d1);
+                    }
+                    tmem_st16(tDS, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+                    tmem_st16(tDS + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar(BAR_DSREADY));
             }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(bar(BAR_DSREADY));
-        }
-        // epilogue: dV and scale * dK of this key, columns [half kD/2, (half+1) kD/2)
-        bool have = ok && steps > 0;
-        if (have) {
-            const bool got = wait_bounded(bar(BAR_ACCDONE), 0, abort_flag, limit);
-            have = __all_sync(0xffffffffu, got);
-            tc_fence_after();
-        }
-        if (ok) {
+            if (!ok) break;
+            // epilogue: dV and scale * dK of this key, columns [half kD/2, (half+1) kD/2).
+            // The accumulators are read out (tcgen05.ld completed) before this
+            // thread's next PREADY, which gates the next item's first dV and dK.
+            bool have = steps > 0;
+            if (have) {
+                const bool got = wait_bounded(bar(BAR_ACCDONE), w & 1, abort_flag, limit);
+                if (!__all_sync(0xffffffffu, got)) break;
+                tc_fence_after();
+            }
             const bool write = key < p.Skv;
-            const size_t off = ((static_cast<size_t>(b) * p.Skv + (write ? key : 0)) * p.Hkv + hkv) * kD + half * (kD / 2);
+            const size_t off =
+                ((static_cast<size_t>(b) * p.Skv + (write ? key : 0)) * p.Hkv + hkv) * kD + half * (kD / 2);
             store_acc_half<kF16, kD>(tmem_base + lane_off + G::kTmemAcc0 + half * (kD / 2), have, 1.f, p.dv + off,
                                      write);
             store_acc_half<kF16, kD>(tmem_base + lane_off + G::kTmemAcc1 + half * (kD / 2), have, p.scale,
                                      p.dk + off, write);
+            if (have) {
+                g += steps;
+                ++w;
+            }
         }
     }
 

@@ -174,10 +174,11 @@ def test_bwd_other_head_dims_unsupported(lib, D):
 
 
 def test_bwd_workspace_size(lib):
-    # two fp32 vectors of B * Hq * (Sq rounded up to 128) entries, each rounded up to 256 bytes
-    assert fa.attn_bwd_workspace_size(1, 256, 256, 2, 2, 128) == 2 * 2 * 256 * 4
-    assert fa.attn_bwd_workspace_size(3, 129, 7, 5, 1, 64) == 2 * 3 * 5 * 256 * 4
-    assert fa.attn_bwd_workspace_size(1, 1, 1, 1, 1, 128) == 2 * 512
+    # two fp32 vectors of B * Hq * (Sq rounded up to 128) entries, each rounded up to 256
+    # bytes, and 256 bytes for the dK/dV kernel's work counter
+    assert fa.attn_bwd_workspace_size(1, 256, 256, 2, 2, 128) == 2 * 2 * 256 * 4 + 256
+    assert fa.attn_bwd_workspace_size(3, 129, 7, 5, 1, 64) == 2 * 3 * 5 * 256 * 4 + 256
+    assert fa.attn_bwd_workspace_size(1, 1, 1, 1, 1, 128) == 2 * 512 + 256
     assert lib.attn_bwd_workspace_size(1, 256, 256, 2, 2, 128, None) == fa.ATTN_ERR_INVALID_ARG
     with pytest.raises(fa.AttnError) as e:
         fa.attn_bwd_workspace_size(1, 256, 256, 3, 2, 128)
