@@ -546,7 +546,8 @@ attn_status_t launch_bwd(const CUtensorMap* tm, const void* o, const void* dO, c
     fmha_bwd_dkdv_kernel<kF16, kD><<<g_kv, kThreads, BwdGeo<kD>::kSmemBytes, stream>>>(tm[0], tm[1], tm[2], tm[3], p);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);
-    const unsigned int g_q = static_cast<unsigned int>(p.B * p.Hq * p.n_q_tiles);
+    const int n_q_items = p.B * p.Hq * p.n_q_tiles;
+    const unsigned int g_q = static_cast<unsigned int>(n_q_items < sms ? n_q_items : sms);
     fmha_bwd_dq_kernel<kF16, kD><<<g_q, kThreads, DqGeo<kD>::kSmemBytes, stream>>>(tm[0], tm[1], tm[2], tm[3], p);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);

@@ -102,7 +102,7 @@ struct BwdParams {
     uint16_t* dq;               // [B, Sq, Hq, D]
     uint16_t* dk;               // [B, Skv, Hkv, D]
     uint16_t* dv;               // [B, Skv, Hkv, D]
-    int* work;                  // work-item counter of the dK/dV kernel (zeroed by prep)
+    int* work;                  // work-item counters of the dK/dV ([0]) and dQ ([1]) kernels (zeroed by prep)
     int n_q_tiles, n_kv_tiles;
     unsigned int poll_limit;
 };
@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(256)
     constexpr int kR = 32 / kL;         // rows per load instruction
     const int lane = static_cast<int>(threadIdx.x) & 31;
     const int b = static_cast<int>(blockIdx.y);
-    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.work = 0;  // the dK/dV kernel's queue
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) p.work[0] = p.work[1] = 0;  // the two queues
     const int per_batch = p.sq_pad * p.Hq;  // rows (i, h) of one batch entry, in memory order
     const int row0 = (static_cast<int>(blockIdx.x) * 8 + static_cast<int>(threadIdx.x) / 32) * (kR * kPrepIters);
     uint4 ov[kPrepIters], dv[kPrepIters];
@@ -394,7 +394,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             const uint64_t pol_fix = l2_policy_evict_first();
             const uint64_t pol_stream = l2_policy_evict_last();
-            int g = 0, w = 0;  // ring fills issued, items with work loaded
+            int g = 0, w = 0;        // ring fills issued, items with work loaded
+            int kfix = 0, vfix = 0;  // K and V fills issued (for the drain)
             for (int j = 0;; ++j) {
                 // take the next item and publish it
                 const int slot = j & 1;
@@ -414,11 +415,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int h = 0; h < G::kHalves; ++h)
                     tma_load_4d(sbase + G::kFix0 + h * kHalfBytes, &tm_k, h * 64, hkv, n * kBN, b, bar(BAR_KFULL),
                                 pol_fix);
+                ++kfix;
                 if (w > 0 && !wait_bounded(bar(BAR_VEMPTY), (w - 1) & 1, abort_flag, limit)) break;
                 mbar_arrive_expect_tx(bar(BAR_VFULL), G::kTileBytes);
                 for (int h = 0; h < G::kHalves; ++h)
                     tma_load_4d(sbase + G::kFix1 + h * kHalfBytes, &tm_v, h * 64, hkv, n * kBN, b, bar(BAR_VFULL),
                                 pol_fix);
+                ++vfix;
                 ++w;
                 bool ok = true;
                 for (int st = 0; st < steps; ++st, ++g) {
@@ -444,10 +447,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
             }
             // drain: every copy issued has landed before the CTA may exit
-            if (w > 0) {
-                drain_bounded(bar(BAR_KFULL), (w - 1) & 1, limit);
-                drain_bounded(bar(BAR_VFULL), (w - 1) & 1, limit);
-            }
+            if (kfix > 0) drain_bounded(bar(BAR_KFULL), (kfix - 1) & 1, limit);
+            if (vfix > 0) drain_bounded(bar(BAR_VFULL), (vfix - 1) & 1, limit);
             for (int s = 0; s < kStages; ++s) {
                 const int fills = g > s ? (g - 1 - s) / kStages + 1 : 0;
                 if (fills) drain_bounded(bar(BAR_FULL + s), (fills - 1) & 1, limit);
@@ -694,29 +695,54 @@ struct DqGeo {
     static constexpr int kBar = kVRing + kVStages * kTileBytes;
     static constexpr int kTmemSlot = kBar + 24 * 8;
     static constexpr int kAbort = kTmemSlot + 4;
-    static constexpr int kSmemBytes = kAbort + 4 + 1024;
+    static constexpr int kItems = kAbort + 4;          // [2] published work items
+    static constexpr int kSmemBytes = kItems + 8 + 1024;
     static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
     static constexpr uint32_t kTmemS = 0, kTmemDP = 128, kTmemDQ = 256;
 };
 
 enum : int {
-    DQB_FIXFULL = 0,
-    DQB_KFULL = 1,        // [K stage]
-    DQB_KEMPTY = 4,       // [K stage]
-    DQB_VFULL = 7,        // [V stage]
-    DQB_VEMPTY = 9,       // [V stage]
-    DQB_SFULL = 11,
+    DQB_QFULL = 0,        // the item's Q landed
+    DQB_QEMPTY,           // its last S completed: Q may be replaced
+    DQB_DOFULL,
+    DQB_DOEMPTY,          // its last dP completed: dO may be replaced
+    DQB_KFULL,            // [K stage]
+    DQB_KEMPTY = DQB_KFULL + 3,
+    DQB_VFULL = DQB_KEMPTY + 3,   // [V stage]
+    DQB_VEMPTY = DQB_VFULL + 2,
+    DQB_SFULL = DQB_VEMPTY + 2,
     DQB_DPFULL,
     DQB_PREADY,           // S_n read out of tensor memory (256 arrivals)
     DQB_DSREADY,          // dS_n in tensor memory (256 arrivals)
-    DQB_ACCDONE,
-    DQB_MMADONE,
+    DQB_ACCDONE,          // the item's last dQ product completed
+    DQB_ITEMFULL,         // [2]
+    DQB_ITEMEMPTY = DQB_ITEMFULL + 2,  // [2]
+    DQB_MMADONE = DQB_ITEMEMPTY + 2,
     DQB_COUNT
 };
 static_assert(DQB_COUNT <= 24, "barrier area");
-// Work item of CTA u: (b, hq) = u / n_q_tiles and its query tile t (last tiles
-// first: under a causal mask they visit the most KV tiles); the CTAs of one
-// head stream the same K/V tiles side by side, out of L2.
+// Work item u = one (b, hq, 128-row query tile), numbered in blocks of
+// kItemHeads query heads: within a block by row tile (under a causal mask the
+// last tiles visit the most KV tiles and go first), then by head, so the CTAs
+// in flight stream the K/V of a few heads (of one GQA group) out of L2.
+__host__ __device__ __forceinline__ void dq_item(const BwdParams& p, int u, int& b, int& hq, int& t) {
+    const int nbh = p.B * p.Hq;
+    const int per_block = kItemHeads * p.n_q_tiles;
+    const int blk = u / per_block;
+    const int within = u - blk * per_block;
+    const int heads = nbh - blk * kItemHeads < kItemHeads ? nbh - blk * kItemHeads : kItemHeads;
+    const int tr = within / heads;
+    const int bh = blk * kItemHeads + (within - tr * heads);
+    t = p.causal ? p.n_q_tiles - 1 - tr : tr;
+    b = bh / p.Hq;
+    hq = bh % p.Hq;
+}
+
+// Persistent, like the dK/dV kernel: items from the second queue, Q and dO of
+// the next item loaded as soon as the current item's last S / dP has read
+// them, K/V rings and per-step barriers running on across items; the next
+// item's first dQ product (which starts the accumulator afresh) waits for the
+// elementwise warps' next dS, issued after they read the accumulator out.
 template <bool kF16, int kD>
 __global__ void __launch_bounds__(kThreads, 1)
     fmha_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -729,20 +755,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) / 32, 0);
     const int lane = static_cast<int>(threadIdx.x) & 31;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + G::kAbort);
+    volatile int* item_slot = reinterpret_cast<volatile int*>(smem + G::kItems);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::kTmemSlot);
     auto bar = [&](int i) -> uint32_t { return sbase + G::kBar + 8 * i; };
-
-    const int u = static_cast<int>(blockIdx.x);
-    const int bh = u / p.n_q_tiles;
-    const int tr = u % p.n_q_tiles;
-    const int t = p.causal ? p.n_q_tiles - 1 - tr : tr;
-    const int b = bh / p.Hq, hq = bh % p.Hq;
-    const int hkv = hq / (p.Hq / p.Hkv);
-    const int nkv = kv_tiles_for_rows(p, t * kBM);
+    const int n_items = p.B * p.Hq * p.n_q_tiles;
     const unsigned int limit = p.poll_limit;
 
     if (warp == kLoadWarp && lane == 0) {
-        mbar_init(bar(DQB_FIXFULL), 1);
+        mbar_init(bar(DQB_QFULL), 1);
+        mbar_init(bar(DQB_QEMPTY), 1);
+        mbar_init(bar(DQB_DOFULL), 1);
+        mbar_init(bar(DQB_DOEMPTY), 1);
         for (int s = 0; s < G::kKStages; ++s) {
             mbar_init(bar(DQB_KFULL + s), 1);
             mbar_init(bar(DQB_KEMPTY + s), 1);
@@ -756,6 +779,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(DQB_PREADY), 32 * kComputeWarps);
         mbar_init(bar(DQB_DSREADY), 32 * kComputeWarps);
         mbar_init(bar(DQB_ACCDONE), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(DQB_ITEMFULL + i), 1);
+            mbar_init(bar(DQB_ITEMEMPTY + i), 1 + kComputeWarps);
+        }
         mbar_init(bar(DQB_MMADONE), 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -775,40 +802,72 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == kLoadWarp) {
         // =========================== TMA producer ===========================
-        if (lane == 0 && nkv > 0) {
+        if (lane == 0) {
             const uint64_t pol_fix = l2_policy_evict_first();
             const uint64_t pol_stream = l2_policy_evict_last();
-            mbar_arrive_expect_tx(bar(DQB_FIXFULL), 2 * G::kTileBytes);
-            for (int h = 0; h < G::kHalves; ++h) {
-                tma_load_4d(sbase + G::kFix0 + h * kHalfBytes, &tm_q, h * 64, hq, t * kBM, b, bar(DQB_FIXFULL),
-                            pol_fix);
-                tma_load_4d(sbase + G::kFix1 + h * kHalfBytes, &tm_do, h * 64, hq, t * kBM, b, bar(DQB_FIXFULL),
-                            pol_fix);
-            }
-            int k_issued = 0, v_issued = 0;
-            for (int kt = 0; kt < nkv; ++kt) {
-                const int ks = kt % G::kKStages, kuse = kt / G::kKStages;
-                if (kuse > 0 && !wait_bounded(bar(DQB_KEMPTY + ks), (kuse - 1) & 1, abort_flag, limit)) break;
-                mbar_arrive_expect_tx(bar(DQB_KFULL + ks), G::kTileBytes);
+            int g = 0, w = 0;          // KV steps loaded, items with work loaded
+            int kf = 0, vf = 0;        // K and V fills issued (for the drain)
+            int qfix = 0, dofix = 0;   // Q and dO fills issued
+            for (int j = 0;; ++j) {
+                const int slot = j & 1;
+                if (j >= 2 && !wait_bounded(bar(DQB_ITEMEMPTY + slot), ((j >> 1) - 1) & 1, abort_flag, limit)) break;
+                int u = *abort_flag ? -1 : atomicAdd(p.work + 1, 1);
+                if (u >= n_items) u = -1;
+                item_slot[slot] = u;
+                mbar_arrive(bar(DQB_ITEMFULL + slot));
+                if (u < 0) break;
+                int b, hq, t;
+                dq_item(p, u, b, hq, t);
+                const int hkv = hq / (p.Hq / p.Hkv);
+                const int nkv = kv_tiles_for_rows(p, t * kBM);
+                if (nkv == 0) continue;
+                if (w > 0 && !wait_bounded(bar(DQB_QEMPTY), (w - 1) & 1, abort_flag, limit)) break;
+                mbar_arrive_expect_tx(bar(DQB_QFULL), G::kTileBytes);
                 for (int h = 0; h < G::kHalves; ++h)
-                    tma_load_4d(sbase + G::kKRing + ks * G::kTileBytes + h * kHalfBytes, &tm_k, h * 64, hkv,
-                                kt * kBN, b, bar(DQB_KFULL + ks), pol_stream);
-                ++k_issued;
-                const int vs = kt % G::kVStages, vuse = kt / G::kVStages;
-                if (vuse > 0 && !wait_bounded(bar(DQB_VEMPTY + vs), (vuse - 1) & 1, abort_flag, limit)) break;
-                mbar_arrive_expect_tx(bar(DQB_VFULL + vs), G::kTileBytes);
+                    tma_load_4d(sbase + G::kFix0 + h * kHalfBytes, &tm_q, h * 64, hq, t * kBM, b, bar(DQB_QFULL),
+                                pol_fix);
+                ++qfix;
+                if (w > 0 && !wait_bounded(bar(DQB_DOEMPTY), (w - 1) & 1, abort_flag, limit)) break;
+                mbar_arrive_expect_tx(bar(DQB_DOFULL), G::kTileBytes);
                 for (int h = 0; h < G::kHalves; ++h)
-                    tma_load_4d(sbase + G::kVRing + vs * G::kTileBytes + h * kHalfBytes, &tm_v, h * 64, hkv,
-                                kt * kBN, b, bar(DQB_VFULL + vs), pol_stream);
-                ++v_issued;
+                    tma_load_4d(sbase + G::kFix1 + h * kHalfBytes, &tm_do, h * 64, hq, t * kBM, b, bar(DQB_DOFULL),
+                                pol_fix);
+                ++dofix;
+                ++w;
+                bool ok = true;
+                for (int kt = 0; kt < nkv; ++kt, ++g) {
+                    const int ks = g % G::kKStages, kuse = g / G::kKStages;
+                    if (kuse > 0 && !wait_bounded(bar(DQB_KEMPTY + ks), (kuse - 1) & 1, abort_flag, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar(DQB_KFULL + ks), G::kTileBytes);
+                    for (int h = 0; h < G::kHalves; ++h)
+                        tma_load_4d(sbase + G::kKRing + ks * G::kTileBytes + h * kHalfBytes, &tm_k, h * 64, hkv,
+                                    kt * kBN, b, bar(DQB_KFULL + ks), pol_stream);
+                    ++kf;
+                    const int vs = g % G::kVStages, vuse = g / G::kVStages;
+                    if (vuse > 0 && !wait_bounded(bar(DQB_VEMPTY + vs), (vuse - 1) & 1, abort_flag, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar(DQB_VFULL + vs), G::kTileBytes);
+                    for (int h = 0; h < G::kHalves; ++h)
+                        tma_load_4d(sbase + G::kVRing + vs * G::kTileBytes + h * kHalfBytes, &tm_v, h * 64, hkv,
+                                    kt * kBN, b, bar(DQB_VFULL + vs), pol_stream);
+                    ++vf;
+                }
+                if (!ok) break;
             }
-            drain_bounded(bar(DQB_FIXFULL), 0, limit);
+            // drain: every copy issued has landed before the CTA may exit
+            if (qfix > 0) drain_bounded(bar(DQB_QFULL), (qfix - 1) & 1, limit);
+            if (dofix > 0) drain_bounded(bar(DQB_DOFULL), (dofix - 1) & 1, limit);
             for (int s = 0; s < G::kKStages; ++s) {
-                const int fills = k_issued > s ? (k_issued - 1 - s) / G::kKStages + 1 : 0;
+                const int fills = kf > s ? (kf - 1 - s) / G::kKStages + 1 : 0;
                 if (fills) drain_bounded(bar(DQB_KFULL + s), (fills - 1) & 1, limit);
             }
             for (int s = 0; s < G::kVStages; ++s) {
-                const int fills = v_issued > s ? (v_issued - 1 - s) / G::kVStages + 1 : 0;
+                const int fills = vf > s ? (vf - 1 - s) / G::kVStages + 1 : 0;
                 if (fills) drain_bounded(bar(DQB_VFULL + s), (fills - 1) & 1, limit);
             }
         }
@@ -824,15 +883,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t k_mn0 = sdesc_sw128(sbase + G::kKRing, kHalfBytes, 1024);
         const uint32_t tS = tmem_base + G::kTmemS, tDP = tmem_base + G::kTmemDP;
         const uint32_t tDQ = tmem_base + G::kTmemDQ;
-        // Issue order S_0, dP_0, then per KV tile n:
+        // Per item, issue order S_0, dP_0, then per KV tile n:
         //   [S_n read out] S_{n+1}, [dS_n stored] dQ_n, dP_{n+1}
         // The elementwise warps signal (PREADY) as soon as S_n is in their
         // registers, so S_{n+1} runs while they form P_n and dS_n; dP_{n+1}
         // overwrites dS_n only after dQ_n (issue order).  A V stage is released
-        // right after its dP, a K stage after its dQ.
-        auto issue_s = [&](int kt) -> bool {  // S of KV tile kt; K_kt must have landed
-            const int ks = kt % G::kKStages;
-            if (!wait_bounded(bar(DQB_KFULL + ks), (kt / G::kKStages) & 1, abort_flag, limit)) return false;
+        // right after its dP, a K stage after its dQ.  g counts KV steps over all
+        // items; PREADY is awaited on every step, including an item's last, so
+        // the next item's S_0 never overwrites an S still being read.
+        auto issue_s = [&](int gk) -> bool {  // S of global KV step gk; its K must have landed
+            const int ks = gk % G::kKStages;
+            if (!wait_bounded(bar(DQB_KFULL + ks), (gk / G::kKStages) & 1, abort_flag, limit)) return false;
             tc_fence_after();
             if (elect_one()) {
                 mma_kmajor<kD>(tS, q_desc, k_k0 + static_cast<uint64_t>((ks * G::kTileBytes) >> 4), idesc_s);
@@ -841,9 +902,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             return true;
         };
-        auto issue_dp = [&](int kt) -> bool {  // dP of KV tile kt; V_kt must have landed
-            const int vs = kt % G::kVStages;
-            if (!wait_bounded(bar(DQB_VFULL + vs), (kt / G::kVStages) & 1, abort_flag, limit)) return false;
+        auto issue_dp = [&](int gk) -> bool {  // dP of global KV step gk; its V must have landed
+            const int vs = gk % G::kVStages;
+            if (!wait_bounded(bar(DQB_VFULL + vs), (gk / G::kVStages) & 1, abort_flag, limit)) return false;
             tc_fence_after();
             if (elect_one()) {
                 mma_kmajor<kD>(tDP, do_desc, v_k0 + static_cast<uint64_t>((vs * G::kTileBytes) >> 4), idesc_s);
@@ -853,23 +914,64 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             return true;
         };
-        bool ok = nkv > 0 && wait_bounded(bar(DQB_FIXFULL), 0, abort_flag, limit) && issue_s(0) && issue_dp(0);
-        for (int kt = 0; ok && kt < nkv; ++kt) {
-            const int ks = kt % G::kKStages;
-            const uint64_t so = static_cast<uint64_t>((ks * G::kTileBytes) >> 4);
-            if (kt + 1 < nkv) {
-                if (!wait_bounded(bar(DQB_PREADY), kt & 1, abort_flag, limit)) break;  // S_kt read out
-                if (!issue_s(kt + 1)) break;
-            }
-            if (!wait_bounded(bar(DQB_DSREADY), kt & 1, abort_flag, limit)) break;
-            tc_fence_after();
-            if (elect_one()) {
-                mma_tmem_mn(tDQ, tDP, k_mn0 + so, idesc_acc, kt > 0);
-                mma_commit(bar(DQB_KEMPTY + ks));
-                if (kt == nkv - 1) mma_commit(bar(DQB_ACCDONE));
-            }
+        auto commit_to = [&](int which) {
+            if (elect_one()) mma_commit(bar(which));
             __syncwarp();
-            if (kt + 1 < nkv && !issue_dp(kt + 1)) break;
+        };
+        bool ok = true;
+        int g = 0, w = 0;
+        for (int j = 0; ok; ++j) {
+            const int slot = j & 1;
+            if (!wait_bounded(bar(DQB_ITEMFULL + slot), (j >> 1) & 1, abort_flag, limit)) break;
+            const int u = item_slot[slot];
+            __syncwarp();
+            if (elect_one()) mbar_arrive(bar(DQB_ITEMEMPTY + slot));
+            __syncwarp();
+            if (u < 0) break;
+            int b, hq, t;
+            dq_item(p, u, b, hq, t);
+            const int nkv = kv_tiles_for_rows(p, t * kBM);
+            if (nkv == 0) continue;
+            // the previous item's last S must have been read out before S_0 overwrites it
+            if (g > 0 && !wait_bounded(bar(DQB_PREADY), (g - 1) & 1, abort_flag, limit)) break;
+            ok = wait_bounded(bar(DQB_QFULL), w & 1, abort_flag, limit) && issue_s(g);
+            if (!ok) break;
+            if (nkv == 1) commit_to(DQB_QEMPTY);
+            ok = wait_bounded(bar(DQB_DOFULL), w & 1, abort_flag, limit) && issue_dp(g);
+            if (!ok) break;
+            if (nkv == 1) commit_to(DQB_DOEMPTY);
+            for (int kt = 0; ok && kt < nkv; ++kt) {
+                const int gk = g + kt;
+                const int ks = gk % G::kKStages;
+                const uint64_t so = static_cast<uint64_t>((ks * G::kTileBytes) >> 4);
+                if (kt + 1 < nkv) {
+                    if (!wait_bounded(bar(DQB_PREADY), gk & 1, abort_flag, limit) || !issue_s(gk + 1)) {
+                        ok = false;
+                        break;
+                    }
+                    if (kt + 2 == nkv) commit_to(DQB_QEMPTY);  // the item's last S is issued
+                }
+                if (!wait_bounded(bar(DQB_DSREADY), gk & 1, abort_flag, limit)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (elect_one()) {
+                    mma_tmem_mn(tDQ, tDP, k_mn0 + so, idesc_acc, kt > 0);
+                    mma_commit(bar(DQB_KEMPTY + ks));
+                    if (kt == nkv - 1) mma_commit(bar(DQB_ACCDONE));
+                }
+                __syncwarp();
+                if (kt + 1 < nkv) {
+                    if (!issue_dp(gk + 1)) {
+                        ok = false;
+                        break;
+                    }
+                    if (kt + 2 == nkv) commit_to(DQB_DOEMPTY);  // the item's last dP is issued
+                }
+            }
+            g += nkv;
+            ++w;
         }
         if (elect_one()) {
             mma_commit(bar(DQB_MMADONE));
@@ -880,76 +982,98 @@ __global__ void __launch_bounds__(kThreads, 1)
         // =========================== elementwise warps ======================
         const int quarter = warp % 4, half = warp / 4;
         const int r = quarter * 32 + lane;  // row within the tile = TMEM lane
-        const int row = t * kBM + r;
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t tS = tmem_base + lane_off + G::kTmemS + 64 * half;
         const uint32_t tDP = tmem_base + lane_off + G::kTmemDP + 64 * half;
         const uint32_t tDS = tmem_base + lane_off + G::kTmemDP + 64 * half;  // packed over own fp32 columns
-        const size_t vo = (static_cast<size_t>(b) * p.Hq + hq) * p.sq_pad + row;  // row < sq_pad
-        const float neg_l2 = -p.lse2[vo];
-        const float dlt = p.delta[vo];
         const float sl2 = p.scale_log2;
-        // last visible key of this row (keys past Skv are masked too)
-        const long long lim_ll = p.causal ? min((long long)row + p.diag, (long long)p.Skv - 1) : (long long)p.Skv - 1;
-        const int lim = static_cast<int>(lim_ll < -1 ? -1 : lim_ll);
         bool ok = true;
-        for (int kt = 0; kt < nkv; ++kt) {
-            const bool got = wait_bounded(bar(DQB_SFULL), kt & 1, abort_flag, limit);
-            if (!__all_sync(0xffffffffu, got)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            uint32_t x[64];
-            tmem_ld64(tS, x);
-            tc_fence_before();
-            mbar_arrive(bar(DQB_PREADY));  // S may now be overwritten by the next tile's product
-            float pv[64];
-#pragma unroll
-            for (int c = 0; c < 64; c += 2) {
-                ffma2_bc(pv[c], pv[c + 1], __uint_as_float(x[c]), __uint_as_float(x[c + 1]), sl2, neg_l2);
-                pv[c] = ex2_approx(pv[c]);
-                pv[c + 1] = ex2_approx(pv[c + 1]);
-            }
-            const int nvis = lim - (kt * kBN + 64 * half) + 1;  // visible columns of this half
-            if (nvis < 64) {
-#pragma unroll
-                for (int c = 0; c < 64; ++c)
-                    if (c >= nvis) pv[c] = 0.f;
-            }
-            const bool got2 = wait_bounded(bar(DQB_DPFULL), kt & 1, abort_flag, limit);
-            if (!__all_sync(0xffffffffu, got2)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            tmem_ld64(tDP, x);
-            {
-                uint32_t pk[32];
+        int g = 0, w = 0;
+        for (int j = 0; ok; ++j) {
+            const int slot = j & 1;
+            const bool got_item = wait_bounded(bar(DQB_ITEMFULL + slot), (j >> 1) & 1, abort_flag, limit);
+            if (!__all_sync(0xffffffffu, got_item)) break;
+            const int u = item_slot[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(DQB_ITEMEMPTY + slot));
+            if (u < 0) break;
+            int b, hq, t;
+            dq_item(p, u, b, hq, t);
+            const int nkv = kv_tiles_for_rows(p, t * kBM);
+            const int row = t * kBM + r;
+            const size_t vo = (static_cast<size_t>(b) * p.Hq + hq) * p.sq_pad + row;  // row < sq_pad
+            const float neg_l2 = -p.lse2[vo];
+            const float dlt = p.delta[vo];
+            // last visible key of this row (keys past Skv are masked too)
+            const long long lim_ll =
+                p.causal ? min((long long)row + p.diag, (long long)p.Skv - 1) : (long long)p.Skv - 1;
+            const int lim = static_cast<int>(lim_ll < -1 ? -1 : lim_ll);
+            for (int kt = 0; kt < nkv; ++kt) {
+                const int gk = g + kt;
+                const bool got = wait_bounded(bar(DQB_SFULL), gk & 1, abort_flag, limit);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t x[64];
+                tmem_ld64(tS, x);
+                tc_fence_before();
+                mbar_arrive(bar(DQB_PREADY));  // S may now be overwritten by the next tile's product
+                float pv[64];
 #pragma unroll
                 for (int c = 0; c < 64; c += 2) {
-                    float d0, d1;
-                    fsubmul2(d0, d1, pv[c], pv[c + 1], __uint_as_float(x[c]), __uint_as_float(x[c + 1]), dlt, dlt);
-                    pk[c / 2] = pack_x2<kF16>(d0, d1);
+                    ffma2_bc(pv[c], pv[c + 1], __uint_as_float(x[c]), __uint_as_float(x[c + 1]), sl2, neg_l2);
+                    pv[c] = ex2_approx(pv[c]);
+                    pv[c + 1] = ex2_approx(pv[c + 1]);
                 }
-                tmem_st16(tDS, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-                tmem_st16(tDS + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+                const int nvis = lim - (kt * kBN + 64 * half) + 1;  // visible columns of this half
+                if (nvis < 64) {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c)
+                        if (c >= nvis) pv[c] = 0.f;
+                }
+                const bool got2 = wait_bounded(bar(DQB_DPFULL), gk & 1, abort_flag, limit);
+                if (!__all_sync(0xffffffffu, got2)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                tmem_ld64(tDP, x);
+                {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int c = 0; c < 64; c += 2) {
+                        float d0, d1;
+                        fsubmul2(d0, d1, pv[c], pv[c + 1], __uint_as_float(x[c]), __uint_as_float(x[c + 1]), dlt,
+                                 dlt);
+                        pk[c / 2] = pack_x2<kF16>(d0, d1);
+                    }
+                    tmem_st16(tDS, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+                    tmem_st16(tDS + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar(DQB_DSREADY));
             }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(bar(DQB_DSREADY));
-        }
-        bool have = ok && nkv > 0;
-        if (have) {
-            const bool got = wait_bounded(bar(DQB_ACCDONE), 0, abort_flag, limit);
-            have = __all_sync(0xffffffffu, got);
-            tc_fence_after();
-        }
-        if (ok) {
+            if (!ok) break;
+            // epilogue: scale * dQ of this row, columns [half kD/2, (half+1) kD/2); the
+            // accumulator is read out before this thread's next DSREADY, which gates
+            // the next item's first dQ product
+            const bool have = nkv > 0;
+            if (have) {
+                const bool got = wait_bounded(bar(DQB_ACCDONE), w & 1, abort_flag, limit);
+                if (!__all_sync(0xffffffffu, got)) break;
+                tc_fence_after();
+            }
             const bool write = row < p.Sq;
             const size_t off = ((static_cast<size_t>(b) * p.Sq + (write ? row : 0)) * p.Hq + hq) * kD + half * (kD / 2);
-            store_acc_half<kF16, kD>(tmem_base + lane_off + G::kTmemDQ + half * (kD / 2), have, p.scale,
-                                     p.dq + off, write);
+            store_acc_half<kF16, kD>(tmem_base + lane_off + G::kTmemDQ + half * (kD / 2), have, p.scale, p.dq + off,
+                                     write);
+            if (have) {
+                g += nkv;
+                ++w;
+            }
         }
     }
 
