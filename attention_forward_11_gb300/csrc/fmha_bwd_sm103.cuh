@@ -39,10 +39,14 @@
 namespace attn {
 namespace bwd {
 
-constexpr int kComputeWarps = 8;
-constexpr int kMmaWarp = 8;
-constexpr int kLoadWarp = 9;
-constexpr int kThreads = 320;
+// The elementwise warps split each 128-column tile into kGroups groups of
+// kCols columns: warp w owns TMEM lane quarter w % 4 and column group w / 4.
+constexpr int kGroups = 2;
+constexpr int kCols = 128 / kGroups;
+constexpr int kComputeWarps = 4 * kGroups;
+constexpr int kMmaWarp = kComputeWarps;
+constexpr int kLoadWarp = kComputeWarps + 1;
+constexpr int kThreads = 32 * (kComputeWarps + 2);
 constexpr int kStages = 2;
 constexpr int kVecBytes = kBM * 4;  // lse2 or delta of one 128-row tile
 
@@ -253,15 +257,41 @@ __device__ __forceinline__ void mma_kmajor(uint32_t d, uint64_t a0, uint64_t b0,
 
 // A from tensor memory (128 lanes x 128 packed 16-bit elements) times an MN-major
 // 128 x kD shared-memory tile: D[128 x kD] (+)= A B.  The packed A is stored as
-// two halves of 64 elements (32 columns each) at columns a_tmem and a_tmem + 64:
-// each elementwise warpgroup packs its half over the start of its own fp32
-// columns, so neither overwrites columns the other is still reading.
+// kGroups pieces of kCols elements (kCols / 2 columns each) at columns
+// a_tmem + kCols * g: each group of elementwise warps packs its piece over the
+// start of its own fp32 columns, so no group overwrites columns another is
+// still reading.
 __device__ __forceinline__ void mma_tmem_mn(uint32_t d, uint32_t a_tmem, uint64_t b0, uint32_t idesc,
                                             bool accumulate) {
+    constexpr int kStepsPerGroup = kCols / 16;
 #pragma unroll
     for (int kk = 0; kk < kBN / 16; ++kk)
-        mma_bf16_ts(d, a_tmem + (kk >> 2) * 64 + (kk & 3) * 8, b0 + static_cast<uint64_t>((kk * 16 * 128) >> 4),
-                    idesc, (accumulate || kk > 0) ? 1u : 0u);
+        mma_bf16_ts(d, a_tmem + (kk / kStepsPerGroup) * kCols + (kk % kStepsPerGroup) * 8,
+                    b0 + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc, (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// kN consecutive fp32 columns of this thread's lane (kN = 16, 32 or 64)
+template <int kN>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[kN]) {
+    if constexpr (kN == 64) {
+        tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+        tmem_ld32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+        tmem_wait_ld_regs(*reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+        tmem_wait_ld_regs(*reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+    } else if constexpr (kN == 32) {
+        tmem_ld32(taddr, r);
+        tmem_wait_ld_regs(r);
+    } else {
+        tmem_ld16(taddr, r);
+        tmem_wait_ld_regs16(r);
+    }
+}
+
+// kN / 2 packed columns (kN = 32 or 64) from registers to tensor memory
+template <int kN>
+__device__ __forceinline__ void tmem_st_packed(uint32_t taddr, const uint32_t (&pk)[kN / 2]) {
+#pragma unroll
+    for (int c = 0; c < kN / 2; c += 16) tmem_st16(taddr + c, *reinterpret_cast<const uint32_t(*)[16]>(&pk[c]));
 }
 
 // 64 consecutive fp32 columns of this thread's lane (two x32 loads)
@@ -272,19 +302,14 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
     tmem_wait_ld_regs(*reinterpret_cast<uint32_t(*)[32]>(&r[32]));
 }
 
-// Accumulator columns [c0, c0 + kD/2) of this thread's lane, times `mul`, to
-// kD/2 16-bit elements at dst (16-byte aligned).
+// kN accumulator columns of this thread's lane from taddr on, times `mul`, to
+// kN 16-bit elements at dst (16-byte aligned); kN = kD / kGroups.
 template <bool kF16, int kD>
-__device__ __forceinline__ void store_acc_half(uint32_t taddr, bool have, float mul, uint16_t* dst, bool write) {
-    constexpr int kN = kD / 2;  // 64 or 32
-    uint32_t a[64];
+__device__ __forceinline__ void store_acc_part(uint32_t taddr, bool have, float mul, uint16_t* dst, bool write) {
+    constexpr int kN = kD / kGroups;  // 16, 32 or 64
+    uint32_t a[kN];
     if (have) {
-        if constexpr (kN == 64) {
-            tmem_ld64(taddr, a);
-        } else {
-            tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&a[0]));
-            tmem_wait_ld_regs(*reinterpret_cast<uint32_t(*)[32]>(&a[0]));
-        }
+        tmem_ld_cols<kN>(taddr, a);
     } else {
 #pragma unroll
         for (int e = 0; e < kN; ++e) a[e] = 0u;
@@ -559,13 +584,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // =========================== elementwise warps ======================
-        const int quarter = warp % 4, half = warp / 4;
+        const int quarter = warp % 4, grp = warp / 4;
         const int jr = quarter * 32 + lane;  // key within the tile = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t tS = tmem_base + lane_off + G::kTmemS + 64 * half;
-        const uint32_t tP = tmem_base + lane_off + G::kTmemS + 64 * half;  // packed over own fp32 columns
-        const uint32_t tDP = tmem_base + lane_off + G::kTmemDP + 64 * half;
-        const uint32_t tDS = tmem_base + lane_off + G::kTmemDP + 64 * half;  // packed over own fp32 columns
+        const uint32_t tS = tmem_base + lane_off + G::kTmemS + kCols * grp;
+        const uint32_t tP = tmem_base + lane_off + G::kTmemS + kCols * grp;  // packed over own fp32 columns
+        const uint32_t tDP = tmem_base + lane_off + G::kTmemDP + kCols * grp;
+        const uint32_t tDS = tmem_base + lane_off + G::kTmemDP + kCols * grp;  // packed over own fp32 columns
         const float sl2 = p.scale_log2;
         bool ok = true;
         int g = 0, w = 0;
@@ -593,16 +618,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const float* l2 = reinterpret_cast<const float*>(smem + G::kVec + s * 2 * kVecBytes) + 64 * half;
+                const float* l2 = reinterpret_cast<const float*>(smem + G::kVec + s * 2 * kVecBytes) + kCols * grp;
                 const float* dl = l2 + kBM;
-                uint32_t x[64];
-                tmem_ld64(tS, x);
+                uint32_t x[kCols];
+                tmem_ld_cols<kCols>(tS, x);
                 // row i = t*128 + 64*half + c sees this key iff key <= i + diag
-                const int row0 = t * kBM + 64 * half;
+                const int row0 = t * kBM + kCols * grp;
                 const int cmin = p.causal ? key - p.diag - row0 : -1;  // first visible column
-                float pv[64];
+                float pv[kCols];
 #pragma unroll
-                for (int c = 0; c < 64; c += 2) {
+                for (int c = 0; c < kCols; c += 2) {
                     ffma2_b(pv[c], pv[c + 1], __uint_as_float(x[c]), __uint_as_float(x[c + 1]), sl2, -l2[c],
                             -l2[c + 1]);
                     pv[c] = ex2_approx(pv[c]);
@@ -610,15 +635,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (cmin > 0) {
 #pragma unroll
-                    for (int c = 0; c < 64; ++c)
+                    for (int c = 0; c < kCols; ++c)
                         if (c < cmin) pv[c] = 0.f;
                 }
                 {
-                    uint32_t pk[32];
+                    uint32_t pk[kCols / 2];
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) pk[c] = pack_x2<kF16>(pv[2 * c], pv[2 * c + 1]);
-                    tmem_st16(tP, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-                    tmem_st16(tP + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+                    for (int c = 0; c < kCols / 2; ++c) pk[c] = pack_x2<kF16>(pv[2 * c], pv[2 * c + 1]);
+                    tmem_st_packed<kCols>(tP, pk);
                 }
                 tmem_wait_st();
                 tc_fence_before();
@@ -629,25 +653,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                tmem_ld64(tDP, x);
+                tmem_ld_cols<kCols>(tDP, x);
                 {
-                    uint32_t pk[32];
+                    uint32_t pk[kCols / 2];
 #pragma unroll
-                    for (int c = 0; c < 64; c += 2) {
+                    for (int c = 0; c < kCols; c += 2) {
                         float d0, d1;
                         fsubmul2(d0, d1, pv[c], pv[c + 1], __uint_as_float(x[c]), __uint_as_float(x[c + 1]), dl[c],
                                  dl[c + 1]);
                         pk[c / 2] = pack_x2<kF16>(d0, d1);
                     }
-                    tmem_st16(tDS, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-                    tmem_st16(tDS + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+                    tmem_st_packed<kCols>(tDS, pk);
                 }
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(bar(BAR_DSREADY));
             }
             if (!ok) break;
-            // epilogue: dV and scale * dK of this key, columns [half kD/2, (half+1) kD/2).
+            // epilogue: dV and scale * dK of this key, columns [grp kD/kGroups, (grp+1) kD/kGroups).
             // The accumulators are read out (tcgen05.ld completed) before this
             // thread's next PREADY, which gates the next item's first dV and dK.
             bool have = steps > 0;
@@ -658,10 +681,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const bool write = key < p.Skv;
             const size_t off =
-                ((static_cast<size_t>(b) * p.Skv + (write ? key : 0)) * p.Hkv + hkv) * kD + half * (kD / 2);
-            store_acc_half<kF16, kD>(tmem_base + lane_off + G::kTmemAcc0 + half * (kD / 2), have, 1.f, p.dv + off,
+                ((static_cast<size_t>(b) * p.Skv + (write ? key : 0)) * p.Hkv + hkv) * kD + grp * (kD / kGroups);
+            store_acc_part<kF16, kD>(tmem_base + lane_off + G::kTmemAcc0 + grp * (kD / kGroups), have, 1.f, p.dv + off,
                                      write);
-            store_acc_half<kF16, kD>(tmem_base + lane_off + G::kTmemAcc1 + half * (kD / 2), have, p.scale,
+            store_acc_part<kF16, kD>(tmem_base + lane_off + G::kTmemAcc1 + grp * (kD / kGroups), have, p.scale,
                                      p.dk + off, write);
             if (have) {
                 g += steps;
@@ -980,12 +1003,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // =========================== elementwise warps ======================
-        const int quarter = warp % 4, half = warp / 4;
+        const int quarter = warp % 4, grp = warp / 4;
         const int r = quarter * 32 + lane;  // row within the tile = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t tS = tmem_base + lane_off + G::kTmemS + 64 * half;
-        const uint32_t tDP = tmem_base + lane_off + G::kTmemDP + 64 * half;
-        const uint32_t tDS = tmem_base + lane_off + G::kTmemDP + 64 * half;  // packed over own fp32 columns
+        const uint32_t tS = tmem_base + lane_off + G::kTmemS + kCols * grp;
+        const uint32_t tDP = tmem_base + lane_off + G::kTmemDP + kCols * grp;
+        const uint32_t tDS = tmem_base + lane_off + G::kTmemDP + kCols * grp;  // packed over own fp32 columns
         const float sl2 = p.scale_log2;
         bool ok = true;
         int g = 0, w = 0;
@@ -1016,21 +1039,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                uint32_t x[64];
-                tmem_ld64(tS, x);
+                uint32_t x[kCols];
+                tmem_ld_cols<kCols>(tS, x);
                 tc_fence_before();
                 mbar_arrive(bar(DQB_PREADY));  // S may now be overwritten by the next tile's product
-                float pv[64];
+                float pv[kCols];
 #pragma unroll
-                for (int c = 0; c < 64; c += 2) {
+                for (int c = 0; c < kCols; c += 2) {
                     ffma2_bc(pv[c], pv[c + 1], __uint_as_float(x[c]), __uint_as_float(x[c + 1]), sl2, neg_l2);
                     pv[c] = ex2_approx(pv[c]);
                     pv[c + 1] = ex2_approx(pv[c + 1]);
                 }
-                const int nvis = lim - (kt * kBN + 64 * half) + 1;  // visible columns of this half
-                if (nvis < 64) {
+                const int nvis = lim - (kt * kBN + kCols * grp) + 1;  // visible columns of this group
+                if (nvis < kCols) {
 #pragma unroll
-                    for (int c = 0; c < 64; ++c)
+                    for (int c = 0; c < kCols; ++c)
                         if (c >= nvis) pv[c] = 0.f;
                 }
                 const bool got2 = wait_bounded(bar(DQB_DPFULL), gk & 1, abort_flag, limit);
@@ -1039,25 +1062,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                tmem_ld64(tDP, x);
+                tmem_ld_cols<kCols>(tDP, x);
                 {
-                    uint32_t pk[32];
+                    uint32_t pk[kCols / 2];
 #pragma unroll
-                    for (int c = 0; c < 64; c += 2) {
+                    for (int c = 0; c < kCols; c += 2) {
                         float d0, d1;
                         fsubmul2(d0, d1, pv[c], pv[c + 1], __uint_as_float(x[c]), __uint_as_float(x[c + 1]), dlt,
                                  dlt);
                         pk[c / 2] = pack_x2<kF16>(d0, d1);
                     }
-                    tmem_st16(tDS, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-                    tmem_st16(tDS + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+                    tmem_st_packed<kCols>(tDS, pk);
                 }
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(bar(DQB_DSREADY));
             }
             if (!ok) break;
-            // epilogue: scale * dQ of this row, columns [half kD/2, (half+1) kD/2); the
+            // epilogue: scale * dQ of this row, columns [grp kD/kGroups, (grp+1) kD/kGroups); the
             // accumulator is read out before this thread's next DSREADY, which gates
             // the next item's first dQ product
             const bool have = nkv > 0;
@@ -1067,8 +1089,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
             }
             const bool write = row < p.Sq;
-            const size_t off = ((static_cast<size_t>(b) * p.Sq + (write ? row : 0)) * p.Hq + hq) * kD + half * (kD / 2);
-            store_acc_half<kF16, kD>(tmem_base + lane_off + G::kTmemDQ + half * (kD / 2), have, p.scale, p.dq + off,
+            const size_t off = ((static_cast<size_t>(b) * p.Sq + (write ? row : 0)) * p.Hq + hq) * kD + grp * (kD / kGroups);
+            store_acc_part<kF16, kD>(tmem_base + lane_off + G::kTmemDQ + grp * (kD / kGroups), have, p.scale, p.dq + off,
                                      write);
             if (have) {
                 g += nkv;
