@@ -247,7 +247,8 @@ def run_reference(args, w):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * metric_flops(w) / (value * 1e12),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {**w.as_dict(), "parallelism": "replicas"},
+        "data": "synthetic",
+        "config": {**w.as_dict(), "parallelism": "replicas" if args.gpus > 1 else "single"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"{rows} random query rows of the workload per step, "
                                    f"~{per_step:.0f} s each; ms_per_step extrapolated to the "
