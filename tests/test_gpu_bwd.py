@@ -249,3 +249,27 @@ def test_bwd_queues_with_mostly_empty_items(Sq, Skv, causal):
         assert np.all(dk[:, Sq:] == 0.0) and np.all(dv[:, Sq:] == 0.0)
     else:
         assert np.all(dq[:, : Sq - Skv] == 0.0)
+
+
+def test_bwd_chunked_prefill_shape_sampled():
+    """B=1, Hq=64, Hkv=8, Sq=512 against Skv=32768 keys, bottom-right mask: dq
+    rows and the dk/dv keys of one key/value head (its 8 query heads)."""
+    _sampled((1, 512, 32768, 64, 8, 128), 1, seed=88, n_rows=32, kv_pairs=[(0, 5)])
+
+
+def test_bwd_long_noncausal_shape_sampled():
+    """B=1, H=16, S=16384 without a mask, Q drawn with sigma 4 (sharp rows)."""
+    B, Sq, Skv, Hq, Hkv, D = 1, 16384, 16384, 16, 16, 128
+    q, k, v, do = problem(B, Sq, Skv, Hq, Hkv, D, seed=89)
+    q = inputs.normal_bf16(q.shape, 4.0, 89, 0)
+    scale = 1 / math.sqrt(D)
+    dq, dk, dv = gpu_grads(q, k, v, do, 0, scale, fwd="gpu")
+    rows = inputs.sample_rows(B, Hq, Sq, 16, 89)
+    ref_dq = oracle.attn_bwd_dq_rows(q, k, v, do, rows, 0, scale)
+    got_dq = np.array([dq[b, i, h] for b, h, i in rows])
+    keys = [(0, 9, j) for j in (0, 1, 127, 128, 8191, 16383)]
+    ref_dk, ref_dv = oracle.attn_bwd_dkv_keys(q, k, v, do, keys, 0, scale)
+    got_dk = np.array([dk[b, j, g] for b, g, j in keys])
+    got_dv = np.array([dv[b, j, g] for b, g, j in keys])
+    compare((got_dq, got_dk, got_dv), (ref_dq, ref_dk, ref_dv), "bf16", "long non-causal sampled",
+            term_sizes(q, k, v, do, scale))
