@@ -15,7 +15,9 @@ Contents
   * ``attn_bwd`` / ``attn_bwd_dq_rows`` / ``attn_bwd_dkv_keys`` -- the C
     oracle's gradients dq, dk, dv of sum(dO * o) in fp64: the plain
     vector-Jacobian product of the definition (the Pallas page's
-    ``_attention_bwd``), for every element or for sampled rows / keys.
+    ``_attention_bwd``), for every element or for sampled rows / keys; on
+    request with delta_i = sum_d dO * o taken from a given 16-bit forward
+    output, as that page's backward kernel takes it from its stored ``out``.
   * ``round_bf16`` -- exact round-to-nearest-even of fp64 values to bf16, the
     comparison value for the bf16 output.
   * ``twin`` (module ``oracle.twin``) -- an independent numpy fp64 restatement
@@ -65,13 +67,13 @@ def configure(lib):
     lib.oracle_partial_triple.argtypes = [P, P, P, L, L, L, L, L, L, ctypes.c_int,
                                           ctypes.c_double, ctypes.c_int, L, L, L, L, L, P, P, P]
     lib.oracle_partial_triple.restype = ctypes.c_int
-    lib.oracle_attn_bwd.argtypes = [P, P, P, P, L, L, L, L, L, L, ctypes.c_int,
+    lib.oracle_attn_bwd.argtypes = [P, P, P, P, P, L, L, L, L, L, L, ctypes.c_int,
                                     ctypes.c_double, ctypes.c_int, P, P, P]
     lib.oracle_attn_bwd.restype = ctypes.c_int
-    lib.oracle_attn_bwd_dq_rows.argtypes = [P, P, P, P, L, L, L, L, L, L, ctypes.c_int,
+    lib.oracle_attn_bwd_dq_rows.argtypes = [P, P, P, P, P, L, L, L, L, L, L, ctypes.c_int,
                                             ctypes.c_double, ctypes.c_int, L, P, P]
     lib.oracle_attn_bwd_dq_rows.restype = ctypes.c_int
-    lib.oracle_attn_bwd_dkv_keys.argtypes = [P, P, P, P, L, L, L, L, L, L, ctypes.c_int,
+    lib.oracle_attn_bwd_dkv_keys.argtypes = [P, P, P, P, P, L, L, L, L, L, L, ctypes.c_int,
                                              ctypes.c_double, ctypes.c_int, L, P, P, P]
     lib.oracle_attn_bwd_dkv_keys.restype = ctypes.c_int
     lib.oracle_num_threads.argtypes = []
@@ -159,15 +161,41 @@ def _check_do(q, do):
         raise ValueError("do must be a C-contiguous uint16 array shaped like q")
 
 
-def attn_bwd(q, k, v, do, causal: int, scale: float, f16: bool = False):
+def _delta_arg(q, do, o, delta, f16):
+    """The delta_i the C entry points are given: None (the exact sum_j p_ij dp_ij),
+    an explicit fp64 [B, Hq, Sq] array, or sum_d do * o over a 16-bit forward
+    output o in q's layout and format (the page's backward takes delta from its
+    stored `out`)."""
+    B, Sq, Hq, D = q.shape
+    if o is not None:
+        if delta is not None:
+            raise ValueError("pass o or delta, not both")
+        if o.dtype != np.uint16 or o.shape != q.shape:
+            raise ValueError("o must be a uint16 array of 16-bit patterns with q's shape")
+        w = f16_bits_to_f64 if f16 else bf16_bits_to_f64
+        delta = np.einsum("bihd,bihd->bhi", w(do), w(o))
+    if delta is None:
+        return None
+    delta = np.ascontiguousarray(np.asarray(delta, dtype=np.float64))
+    if delta.shape != (B, Hq, Sq):
+        raise ValueError("delta must be [B, Hq, Sq]")
+    return delta
+
+
+def attn_bwd(q, k, v, do, causal: int, scale: float, f16: bool = False, o=None, delta=None):
     """fp64 (dq [B,Sq,Hq,D], dk [B,Skv,Hkv,D], dv [B,Skv,Hkv,D]): the gradient of
-    sum(do * o) with o the attention output; do has q's shape and 16-bit format."""
+    sum(do * o) with o the attention output; do has q's shape and 16-bit format.
+    By default delta_i = sum_j p_ij dp_ij (exact).  o: a 16-bit forward output
+    (q's layout and format) to take delta_i = sum_d do * o from, as a backward
+    given the stored output does; delta: explicit fp64 [B, Hq, Sq] values."""
     B, Sq, Skv, Hq, Hkv, D = _check_inputs(q, k, v)
     _check_do(q, do)
+    dl = _delta_arg(q, do, o, delta, f16)
     dq = np.zeros((B, Sq, Hq, D), dtype=np.float64)
     dk = np.zeros((B, Skv, Hkv, D), dtype=np.float64)
     dv = np.zeros((B, Skv, Hkv, D), dtype=np.float64)
-    rc = _load().oracle_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(do), B, Sq, Skv, Hq, Hkv, D,
+    rc = _load().oracle_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(do),
+                                 None if dl is None else _ptr(dl), B, Sq, Skv, Hq, Hkv, D,
                                  int(causal), float(scale), int(bool(f16)), _ptr(dq), _ptr(dk),
                                  _ptr(dv))
     if rc != 0:
@@ -175,13 +203,16 @@ def attn_bwd(q, k, v, do, causal: int, scale: float, f16: bool = False):
     return dq, dk, dv
 
 
-def attn_bwd_dq_rows(q, k, v, do, rows, causal: int, scale: float, f16: bool = False):
-    """fp64 dq (len(rows) x D) of the listed (b, h, i) rows."""
+def attn_bwd_dq_rows(q, k, v, do, rows, causal: int, scale: float, f16: bool = False, o=None,
+                     delta=None):
+    """fp64 dq (len(rows) x D) of the listed (b, h, i) rows; o, delta as for attn_bwd."""
     B, Sq, Skv, Hq, Hkv, D = _check_inputs(q, k, v)
     _check_do(q, do)
+    dl = _delta_arg(q, do, o, delta, f16)
     rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
     dq = np.zeros((rows.shape[0], D), dtype=np.float64)
-    rc = _load().oracle_attn_bwd_dq_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(do), B, Sq, Skv, Hq,
+    rc = _load().oracle_attn_bwd_dq_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(do),
+                                         None if dl is None else _ptr(dl), B, Sq, Skv, Hq,
                                          Hkv, D, int(causal), float(scale), int(bool(f16)),
                                          rows.shape[0], _ptr(rows), _ptr(dq))
     if rc != 0:
@@ -189,14 +220,18 @@ def attn_bwd_dq_rows(q, k, v, do, rows, causal: int, scale: float, f16: bool = F
     return dq
 
 
-def attn_bwd_dkv_keys(q, k, v, do, keys, causal: int, scale: float, f16: bool = False):
-    """fp64 (dk, dv), each len(keys) x D, of the listed (b, g, j) keys (g: key/value head)."""
+def attn_bwd_dkv_keys(q, k, v, do, keys, causal: int, scale: float, f16: bool = False, o=None,
+                      delta=None):
+    """fp64 (dk, dv), each len(keys) x D, of the listed (b, g, j) keys (g: key/value
+    head); o, delta as for attn_bwd."""
     B, Sq, Skv, Hq, Hkv, D = _check_inputs(q, k, v)
     _check_do(q, do)
+    dl = _delta_arg(q, do, o, delta, f16)
     keys = np.ascontiguousarray(np.asarray(keys, dtype=np.int64).reshape(-1, 3))
     dk = np.zeros((keys.shape[0], D), dtype=np.float64)
     dv = np.zeros((keys.shape[0], D), dtype=np.float64)
-    rc = _load().oracle_attn_bwd_dkv_keys(_ptr(q), _ptr(k), _ptr(v), _ptr(do), B, Sq, Skv, Hq,
+    rc = _load().oracle_attn_bwd_dkv_keys(_ptr(q), _ptr(k), _ptr(v), _ptr(do),
+                                          None if dl is None else _ptr(dl), B, Sq, Skv, Hq,
                                           Hkv, D, int(causal), float(scale), int(bool(f16)),
                                           keys.shape[0], _ptr(keys), _ptr(dk), _ptr(dv))
     if rc != 0:

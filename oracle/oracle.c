@@ -50,6 +50,11 @@
  * The page's backward rejects the causal mask; these functions apply the same
  * visibility rule as the forward (a masked pair has p_ij = 0), the gradient of
  * the masked forward.
+ * The page's backward kernel takes delta_i from the stored forward output
+ * (its residual `out`, in the input's element type) rather than from the
+ * exact o_i.  Each backward entry point therefore also accepts delta_i from
+ * the caller (delta_in, [B,Hq,Sq]); dq, dk, dv are affine in it and the
+ * other quantities are unchanged.
  */
 #include <math.h>
 #include <stdint.h>
@@ -257,10 +262,11 @@ int oracle_partial_triple(const uint16_t *q, const uint16_t *k, const uint16_t *
  * ds_buf[j] = ds_ij for j < *end_out (the row's visible keys), and, if dq is not
  * NULL, dq[0..D) = scale * sum_j ds_ij k_j.  qd, dod: D doubles of scratch.
  * Three passes over the keys: logits and their max; weights, lse and dp_ij with
- * delta_i; ds_ij and dq. */
-static void row_grad(const problem_t *p, const uint16_t *dO, long b, long h, long i,
-                     double *p_buf, double *ds_buf, double *qd, double *dod, double *dq,
-                     long *end_out) {
+ * delta_i = sum_j p_ij dp_ij; ds_ij and dq.  delta_in (NULL: the exact delta_i
+ * above) supplies delta_i instead, indexed [(b * Hq + h) * Sq + i]. */
+static void row_grad(const problem_t *p, const uint16_t *dO, const double *delta_in, long b,
+                     long h, long i, double *p_buf, double *ds_buf, double *qd, double *dod,
+                     double *dq, long *end_out) {
     const long D = p->D;
     const long g = h / (p->Hq / p->Hkv);
     const long end = visible_end(p, i);
@@ -295,6 +301,7 @@ static void row_grad(const problem_t *p, const uint16_t *dO, long b, long h, lon
         ds_buf[j] = dp;
         delta += p_buf[j] * dp;
     }
+    if (delta_in) delta = delta_in[(b * p->Hq + h) * p->Sq + i];
     /* pass 3: ds_ij and dq */
     for (long j = 0; j < end; ++j) {
         ds_buf[j] = p_buf[j] * (ds_buf[j] - delta);
@@ -308,13 +315,15 @@ static void row_grad(const problem_t *p, const uint16_t *dO, long b, long h, lon
 }
 
 /*
- * Every gradient.  dO: [B,Sq,Hq,D] 16-bit patterns in q's format.
+ * Every gradient.  dO: [B,Sq,Hq,D] 16-bit patterns in q's format; delta_in:
+ * NULL (exact delta_i) or [B,Hq,Sq] doubles (see row_grad).
  * dq_out: [B,Sq,Hq,D] doubles; dk_out, dv_out: [B,Skv,Hkv,D] doubles.
  * Parallel over (b, g): each thread owns the dk/dv rows of its key/value head.
  */
 int oracle_attn_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *dO,
-                    long B, long Sq, long Skv, long Hq, long Hkv, long D, int causal,
-                    double scale, int f16, double *dq_out, double *dk_out, double *dv_out) {
+                    const double *delta_in, long B, long Sq, long Skv, long Hq, long Hkv, long D,
+                    int causal, double scale, int f16, double *dq_out, double *dk_out,
+                    double *dv_out) {
     if (check_dims(B, Sq, Skv, Hq, Hkv, D) || causal < 0 || causal > 2) return -1;
     problem_t p = {q, k, v, B, Sq, Skv, Hq, Hkv, D, causal, scale, f16 != 0};
     const long G = Hq / Hkv;
@@ -341,7 +350,7 @@ int oracle_attn_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, con
                     for (long i = 0; i < Sq; ++i) {
                         long end;
                         double *dq = dq_out + ((b * Sq + i) * Hq + h) * D;
-                        row_grad(&p, dO, b, h, i, p_buf, ds_buf, qd, dod, dq, &end);
+                        row_grad(&p, dO, delta_in, b, h, i, p_buf, ds_buf, qd, dod, dq, &end);
                         for (long j = 0; j < end; ++j) {
                             double *dk = dk_out + ((b * Skv + j) * Hkv + g) * D;
                             double *dv = dv_out + ((b * Skv + j) * Hkv + g) * D;
@@ -363,11 +372,11 @@ int oracle_attn_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, con
 
 /*
  * dq of an explicit list of rows: rows holds nrows triples (b, h, i);
- * dq_out: nrows*D doubles.
+ * dq_out: nrows*D doubles; delta_in as for oracle_attn_bwd.
  */
 int oracle_attn_bwd_dq_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                            const uint16_t *dO, long B, long Sq, long Skv, long Hq, long Hkv,
-                            long D, int causal, double scale, int f16, long nrows,
+                            const uint16_t *dO, const double *delta_in, long B, long Sq, long Skv,
+                            long Hq, long Hkv, long D, int causal, double scale, int f16, long nrows,
                             const long *rows, double *dq_out) {
     if (check_dims(B, Sq, Skv, Hq, Hkv, D) || causal < 0 || causal > 2) return -1;
     problem_t p = {q, k, v, B, Sq, Skv, Hq, Hkv, D, causal, scale, f16 != 0};
@@ -391,8 +400,8 @@ int oracle_attn_bwd_dq_rows(const uint16_t *q, const uint16_t *k, const uint16_t
             for (long r = 0; r < nrows; ++r) {
                 const long *t = rows + 3 * r;
                 long end;
-                row_grad(&p, dO, t[0], t[1], t[2], p_buf, ds_buf, qd, dod, dq_out + r * D,
-                         &end);
+                row_grad(&p, dO, delta_in, t[0], t[1], t[2], p_buf, ds_buf, qd, dod,
+                         dq_out + r * D, &end);
             }
         }
         free(p_buf);
@@ -408,11 +417,11 @@ int oracle_attn_bwd_dq_rows(const uint16_t *q, const uint16_t *k, const uint16_t
  * with g a key/value head; dk_out, dv_out: nkeys*D doubles each.  For every
  * (b, g) that occurs, the per-row lse_i and delta_i of the group's query heads
  * are computed once (one row pass each), then each listed key sums over the
- * rows that see it.
+ * rows that see it.  delta_in as for oracle_attn_bwd.
  */
 int oracle_attn_bwd_dkv_keys(const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                             const uint16_t *dO, long B, long Sq, long Skv, long Hq, long Hkv,
-                             long D, int causal, double scale, int f16, long nkeys,
+                             const uint16_t *dO, const double *delta_in, long B, long Sq, long Skv,
+                             long Hq, long Hkv, long D, int causal, double scale, int f16, long nkeys,
                              const long *keys, double *dk_out, double *dv_out) {
     if (check_dims(B, Sq, Skv, Hq, Hkv, D) || causal < 0 || causal > 2) return -1;
     problem_t p = {q, k, v, B, Sq, Skv, Hq, Hkv, D, causal, scale, f16 != 0};
@@ -474,7 +483,7 @@ int oracle_attn_bwd_dkv_keys(const uint16_t *q, const uint16_t *k, const uint16_
                         dl += exp(p_buf[j] - ls) * dp;
                     }
                     lse[hi] = ls;
-                    delta[hi] = dl;
+                    delta[hi] = delta_in ? delta_in[(b * Hq + h) * Sq + i] : dl;
                 }
             }
             free(p_buf);

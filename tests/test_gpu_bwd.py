@@ -1,27 +1,34 @@
 """GPU parity of the backward pass (attn_bwd, through the C ABI) against the fp64
 oracle's gradients of sum(dO * O).
 
+Reference.  attn_bwd forms delta_i = sum_d dO * O from the 16-bit O it is
+given, as the Pallas page's backward takes delta from its stored `out`.  The
+tests therefore compare with the oracle's gradient for that same delta
+(`oracle.attn_bwd(..., o=...)`, pinned against the exact gradient by the
+delta-identity and delta-shift pins).  The exact gradient differs from it by
+the rounding of O itself: dq_i moves by -scale * ddelta_i * sum_j p_ij k_j,
+with ddelta_i = sum_d dO * (O - o_exact), and dk by the matching sum over
+rows.  That term is largest in rows that see two or three keys, where nothing
+averages it down.  On the full headline shape it reaches 47 u rms of dq.
+test_bwd_after_gpu_forward compares the forward-then-backward pipeline with
+the exact gradient on shapes where it stays within the bound below.
+
 Tolerance.  With u the unit roundoff of the element type (2^-8 for bf16,
 2^-11 for binary16) and rms the root-mean-square of the oracle's gradient tensor
 over the compared elements it does not make exactly zero:
     mean |g - g_oracle| <= 1 u rms      |g - g_oracle| <= 40 u rms + 2 u |g_oracle|
 The kernels round P and dS to the element type before each product and the
-outputs once at the end; O (used for delta) arrives rounded too.  Each of those
-roundings moves one term of a gradient sum by at most u of itself, so the error
-of an element is a sum of many independent terms of size <= u |term|: its mean
-over a tensor stays below u rms, and the largest of ~10^5 elements stays well
-below 40 u rms -- plus 2 u of the element itself, for the output's own rounding
-and a dominant term's (elements far above the rms, as in a sparse dv, round on
-their own scale).  A wrong scale, sign, delta or mask moves elements by O(rms),
-hundreds of u.
+outputs once at the end.  Each of those roundings moves one term of a
+gradient sum by at most u of itself, so the error of an element is a sum of
+many independent terms of size <= u |term|.  Its mean over a tensor stays
+below u rms, and the largest of ~10^8 elements stays below 40 u rms, plus 2 u
+of the element itself for the output's own rounding and a dominant term's
+(elements far above the rms, as in a sparse dv, round on their own scale).
+A wrong scale, sign, delta or mask moves elements by O(rms), hundreds of u.
 
 Inputs.  Most cases hand attn_bwd the oracle's O (correctly rounded) and LSE,
-so they test the backward kernels alone.  delta = rowsum(dO * O) is formed from
-the O it is given (as in the Pallas page's backward); the forward's O may sit
-an ulp off the correctly rounded value (within its own tolerance), and where
-dS = P (dP - delta) cancels exactly -- rows that see a single key -- that ulp is
-the whole of dq and dk.  The forward-to-backward pipeline is checked on shapes
-without such rows (test_bwd_after_gpu_forward and the full-size samples).
+so they test the backward kernels alone; the pipeline and full-size sampled
+tests take O and LSE from attn_fwd.
 """
 import math
 
@@ -56,16 +63,18 @@ def oracle_forward_bits(q, k, v, causal, scale, dtype="bf16"):
     return np.ascontiguousarray(o_bits), lse.astype(np.float32)
 
 
-def gpu_grads(q, k, v, do, causal, scale, dtype="bf16", raw=False, fwd="oracle"):
+def gpu_grads(q, k, v, do, causal, scale, dtype="bf16", raw=False, fwd="oracle", want_o=False):
     """dq, dk, dv from attn_bwd (fp64 numpy, or the device tensors with raw=True).
     fwd="oracle": O and LSE are the oracle's (O correctly rounded), which tests
     the backward kernels on exact inputs; fwd="gpu": they come from attn_fwd, the
-    pipeline a training step runs."""
+    pipeline a training step runs.  want_o: also return the 16-bit O patterns
+    attn_bwd was given (numpy uint16, q's layout)."""
     import torch
     import attention_forward_11_gb300 as fa
     tq, tk, tv, tdo = (to_device(x, dtype) for x in (q, k, v, do))
     if fwd == "gpu":
         o, lse = fa.attn_fwd(tq, tk, tv, causal=int(causal), scale=scale)
+        o_bits = o.view(torch.int16).cpu().numpy().view(np.uint16) if want_o else None
     else:
         o_bits, lse_np = oracle_forward_bits(q, k, v, causal, scale, dtype)
         o, lse = to_device(o_bits, dtype), torch.from_numpy(lse_np).cuda()
@@ -75,7 +84,7 @@ def gpu_grads(q, k, v, do, causal, scale, dtype="bf16", raw=False, fwd="oracle")
         return dq, dk, dv
     out = tuple(t.float().double().cpu().numpy() for t in (dq, dk, dv))
     torch.cuda.synchronize()
-    return out
+    return (out, o_bits) if want_o else out
 
 
 def term_sizes(q, k, v, do, scale, dtype="bf16"):
@@ -112,10 +121,12 @@ def compare(got, ref, dtype, what, terms):
         assert excess.max() <= MAX_U * u * norm, f"{what} {name}: max err {excess.max() / norm:.3e} rms"
 
 
-def check(q, k, v, do, causal, scale, what, dtype="bf16", fwd="oracle"):
-    compare(gpu_grads(q, k, v, do, causal, scale, dtype=dtype, fwd=fwd),
-            oracle.attn_bwd(q, k, v, do, causal, scale, f16=dtype == "f16"), dtype, what,
-            term_sizes(q, k, v, do, scale, dtype))
+def check(q, k, v, do, causal, scale, what, dtype="bf16", fwd="oracle", exact=False):
+    """Every element against the oracle: the gradient for the delta of the O
+    attn_bwd was given, or (exact=True) the exact gradient."""
+    got, o_bits = gpu_grads(q, k, v, do, causal, scale, dtype=dtype, fwd=fwd, want_o=True)
+    ref = oracle.attn_bwd(q, k, v, do, causal, scale, f16=dtype == "f16", o=None if exact else o_bits)
+    compare(got, ref, dtype, what, term_sizes(q, k, v, do, scale, dtype))
 
 
 CASES = [
@@ -145,9 +156,12 @@ def test_bwd_matches_oracle(case):
                                   (1, 1000, 1000, 2, 1, 128, 0), (1, 384, 384, 2, 2, 64, 1)],
                          ids=lambda c: "B{}_Sq{}_Skv{}_H{}-{}_D{}_c{}".format(*c))
 def test_bwd_after_gpu_forward(case):
-    """O and LSE from attn_fwd, as a training step runs them."""
+    """O and LSE from attn_fwd, as a training step runs them, against the exact
+    gradient (O's rounding included in the error) and against the gradient for
+    the delta of that O."""
     *shape, causal = case
     q, k, v, do = problem(*shape, seed=sum(case) + 1)
+    check(q, k, v, do, causal, 1 / math.sqrt(shape[5]), str(case), fwd="gpu", exact=True)
     check(q, k, v, do, causal, 1 / math.sqrt(shape[5]), str(case), fwd="gpu")
 
 
@@ -207,9 +221,9 @@ def _sampled(shape, causal, seed, n_rows, kv_pairs, dtype="bf16"):
     B, Sq, Skv, Hq, Hkv, D = shape
     q, k, v, do = problem(*shape, seed=seed, dtype=dtype)
     scale = 1 / math.sqrt(D)
-    dq, dk, dv = gpu_grads(q, k, v, do, causal, scale, dtype=dtype, fwd="gpu")
+    (dq, dk, dv), o_bits = gpu_grads(q, k, v, do, causal, scale, dtype=dtype, fwd="gpu", want_o=True)
     rows = inputs.sample_rows(B, Hq, Sq, n_rows, seed)
-    ref_dq = oracle.attn_bwd_dq_rows(q, k, v, do, rows, causal, scale, f16=dtype == "f16")
+    ref_dq = oracle.attn_bwd_dq_rows(q, k, v, do, rows, causal, scale, f16=dtype == "f16", o=o_bits)
     got_dq = np.array([dq[b, i, h] for b, h, i in rows])
     rng = np.random.default_rng(seed)
     keys = []
@@ -217,7 +231,8 @@ def _sampled(shape, causal, seed, n_rows, kv_pairs, dtype="bf16"):
         js = {0, 1, 127, 128, Skv // 2, Skv - 129, Skv - 128, Skv - 1}
         js.update(rng.integers(0, Skv, 12).tolist())
         keys += [(b, g, j) for j in sorted(js) if 0 <= j < Skv]
-    ref_dk, ref_dv = oracle.attn_bwd_dkv_keys(q, k, v, do, keys, causal, scale, f16=dtype == "f16")
+    ref_dk, ref_dv = oracle.attn_bwd_dkv_keys(q, k, v, do, keys, causal, scale, f16=dtype == "f16",
+                                              o=o_bits)
     got_dk = np.array([dk[b, j, g] for b, g, j in keys])
     got_dv = np.array([dv[b, j, g] for b, g, j in keys])
     compare((got_dq, got_dk, got_dv), (ref_dq, ref_dk, ref_dv), dtype, f"{shape} sampled",
@@ -228,6 +243,15 @@ def test_bwd_headline_shape_sampled():
     """B=4, H=16, S=4096, D=128, causal (the forward's headline shape): sampled
     dq rows and dk/dv keys of two (batch, head) pairs against the oracle."""
     _sampled((4, 4096, 4096, 16, 16, 128), 1, seed=86, n_rows=48, kv_pairs=[(0, 0), (3, 15)])
+
+
+def test_bwd_headline_shape_every_element():
+    """The same shape with every element of dq, dk and dv against the oracle's
+    full backward (about 0.7 TFLOP of fp64 work over the host's cores), the
+    kernels given the oracle's O (correctly rounded) and LSE."""
+    B, S, H, D = 4, 4096, 16, 128
+    q, k, v, do = problem(B, S, S, H, H, D, seed=90)
+    check(q, k, v, do, 1, 1 / math.sqrt(D), "headline every element")
 
 
 def test_bwd_gqa_sampled():
@@ -263,12 +287,12 @@ def test_bwd_long_noncausal_shape_sampled():
     q, k, v, do = problem(B, Sq, Skv, Hq, Hkv, D, seed=89)
     q = inputs.normal_bf16(q.shape, 4.0, 89, 0)
     scale = 1 / math.sqrt(D)
-    dq, dk, dv = gpu_grads(q, k, v, do, 0, scale, fwd="gpu")
+    (dq, dk, dv), o_bits = gpu_grads(q, k, v, do, 0, scale, fwd="gpu", want_o=True)
     rows = inputs.sample_rows(B, Hq, Sq, 16, 89)
-    ref_dq = oracle.attn_bwd_dq_rows(q, k, v, do, rows, 0, scale)
+    ref_dq = oracle.attn_bwd_dq_rows(q, k, v, do, rows, 0, scale, o=o_bits)
     got_dq = np.array([dq[b, i, h] for b, h, i in rows])
     keys = [(0, 9, j) for j in (0, 1, 127, 128, 8191, 16383)]
-    ref_dk, ref_dv = oracle.attn_bwd_dkv_keys(q, k, v, do, keys, 0, scale)
+    ref_dk, ref_dv = oracle.attn_bwd_dkv_keys(q, k, v, do, keys, 0, scale, o=o_bits)
     got_dk = np.array([dk[b, j, g] for b, g, j in keys])
     got_dv = np.array([dv[b, j, g] for b, g, j in keys])
     compare((got_dq, got_dk, got_dv), (ref_dq, ref_dk, ref_dv), "bf16", "long non-causal sampled",

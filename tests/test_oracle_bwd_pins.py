@@ -222,3 +222,73 @@ def test_bwd_fully_masked_rows_contribute_nothing():
     np.testing.assert_array_equal(dk, dk2)
     np.testing.assert_array_equal(dv, dv2)
     np.testing.assert_array_equal(dq, dq2)
+
+
+@pytest.mark.parametrize("causal", [0, 1, 2])
+def test_bwd_supplied_delta_equal_to_exact(causal):
+    """delta_i supplied as dO_i . o_i, with o the oracle forward's exact fp64 output,
+    reproduces the exact gradient in every entry point (the identity
+    sum_j p_ij dp_ij = dO_i . o_i); rows that see no key have o = 0."""
+    B, Sq, Skv, Hq, Hkv, D = 2, 12, 9, 4, 2, 8
+    q, k, v, do = _problem(B, Sq, Skv, Hq, Hkv, D, seed=70 + causal)
+    o, _ = oracle.attn_full(q, k, v, causal, 0.3)
+    delta = np.einsum("bihd,bihd->bhi", _widen(do), o)
+    exact = oracle.attn_bwd(q, k, v, do, causal, 0.3)
+    given = oracle.attn_bwd(q, k, v, do, causal, 0.3, delta=delta)
+    for a, b in zip(exact, given):
+        np.testing.assert_allclose(b, a, rtol=1e-10, atol=1e-13)
+    rows = [(1, 3, 0), (0, 2, 5), (1, 0, Sq - 1)]
+    np.testing.assert_allclose(oracle.attn_bwd_dq_rows(q, k, v, do, rows, causal, 0.3, delta=delta),
+                               np.array([exact[0][b, i, h] for b, h, i in rows]), rtol=1e-10, atol=1e-13)
+    keys = [(0, 1, 0), (1, 0, Skv - 1), (1, 1, 4)]
+    gk, gv = oracle.attn_bwd_dkv_keys(q, k, v, do, keys, causal, 0.3, delta=delta)
+    np.testing.assert_allclose(gk, np.array([exact[1][b, j, g] for b, g, j in keys]), rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(gv, np.array([exact[2][b, j, g] for b, g, j in keys]), rtol=1e-10, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [0, 1, 2])
+def test_bwd_delta_shift(causal):
+    """The gradients are affine in delta with the slopes of the softmax Jacobian:
+    moving delta_i by e_i moves dq_i by -scale e_i sum_j p_ij k_j (the oracle's
+    forward with v := k), moves dk_j by -scale sum_i p_ij e_i q_i (the exact
+    backward's dv for dO_i := e_i q_i, exact in bf16 because every e_i is 0 or a
+    power of two) and leaves dv unchanged.  Every entry point takes the same delta."""
+    B, Sq, Skv, Hq, Hkv, D, scale = 1, 10, 7, 4, 2, 8, 0.3
+    q, k, v, do = _problem(B, Sq, Skv, Hq, Hkv, D, seed=80 + causal)
+    rng = np.random.default_rng(causal)
+    e = rng.choice([-1.0, -0.5, 0.0, 0.25, 2.0], size=(B, Hq, Sq))
+    o, _ = oracle.attn_full(q, k, v, causal, scale)
+    delta = np.einsum("bihd,bihd->bhi", _widen(do), o)
+    base = oracle.attn_bwd(q, k, v, do, causal, scale, delta=delta)
+    moved = oracle.attn_bwd(q, k, v, do, causal, scale, delta=delta + e)
+    pk, _ = oracle.attn_full(q, k, k, causal, scale)
+    e_rows = e.transpose(0, 2, 1)[..., None]  # [B, Sq, Hq, 1]
+    np.testing.assert_allclose(moved[0] - base[0], -scale * e_rows * pk, rtol=1e-9, atol=1e-12)
+    eq = e_rows * _widen(q)
+    do2 = inputs.f32_to_bf16_bits(eq.astype(np.float32))
+    np.testing.assert_array_equal(_widen(do2), eq)
+    _, _, dv2 = oracle.attn_bwd(q, k, v, do2, causal, scale)
+    np.testing.assert_allclose(moved[1] - base[1], -scale * dv2, rtol=1e-9, atol=1e-12)
+    np.testing.assert_array_equal(moved[2], base[2])
+    rows = [(0, h, i) for h in range(Hq) for i in range(Sq)]
+    np.testing.assert_allclose(oracle.attn_bwd_dq_rows(q, k, v, do, rows, causal, scale, delta=delta + e),
+                               np.array([moved[0][b, i, h] for b, h, i in rows]), rtol=1e-10, atol=1e-13)
+    keys = [(0, g, j) for g in range(Hkv) for j in range(Skv)]
+    gk, _ = oracle.attn_bwd_dkv_keys(q, k, v, do, keys, causal, scale, delta=delta + e)
+    np.testing.assert_allclose(gk, np.array([moved[1][b, j, g] for b, g, j in keys]), rtol=1e-10, atol=1e-13)
+
+
+def test_bwd_delta_from_output_bits():
+    """o= takes delta_i = sum_d dO . o from the 16-bit output, the same numbers as
+    passing that sum explicitly; o and delta together are refused."""
+    B, Sq, Skv, Hq, Hkv, D = 1, 6, 6, 2, 1, 8
+    q, k, v, do = _problem(B, Sq, Skv, Hq, Hkv, D, seed=90)
+    o, _ = oracle.attn_full(q, k, v, 1, 0.4)
+    o_bits = inputs.f32_to_bf16_bits(oracle.round_bf16(o).astype(np.float32))
+    d = np.einsum("bihd,bihd->bhi", _widen(do), _widen(o_bits))
+    a = oracle.attn_bwd(q, k, v, do, 1, 0.4, o=o_bits)
+    b = oracle.attn_bwd(q, k, v, do, 1, 0.4, delta=d)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+    with pytest.raises(ValueError):
+        oracle.attn_bwd(q, k, v, do, 1, 0.4, o=o_bits, delta=d)

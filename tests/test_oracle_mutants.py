@@ -60,6 +60,11 @@ MUTANTS = [
      "const double ds = pij * (dp + delta[hi]);"),
     ("bwd_keys_mask_off_by_one", "if (j >= visible_end(&p, i)) continue;",
      "if (j > visible_end(&p, i)) continue;"),
+    ("bwd_supplied_delta_ignored", "if (delta_in) delta = delta_in[(b * p->Hq + h) * p->Sq + i];", ";"),
+    ("bwd_supplied_delta_row_major", "if (delta_in) delta = delta_in[(b * p->Hq + h) * p->Sq + i];",
+     "if (delta_in) delta = delta_in[(b * p->Sq + i) * p->Hq + h];"),
+    ("bwd_keys_supplied_delta_ignored", "delta[hi] = delta_in ? delta_in[(b * Hq + h) * Sq + i] : dl;",
+     "delta[hi] = dl;"),
 ]
 
 PIN_TESTS = [
@@ -76,7 +81,8 @@ BWD_PIN_TESTS = [
     "test_bwd_hand_worked_two_keys", "test_bwd_zero_query_closed_form",
     "test_bwd_constant_values_give_zero_dq_dk", "test_bwd_invariants",
     "test_bwd_gqa_equals_repeated_heads", "test_bwd_sampled_entry_points_match_full",
-    "test_bwd_fully_masked_rows_contribute_nothing",
+    "test_bwd_fully_masked_rows_contribute_nothing", "test_bwd_supplied_delta_equal_to_exact",
+    "test_bwd_delta_shift",
 ]
 
 
