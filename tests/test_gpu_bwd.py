@@ -103,8 +103,10 @@ def compare(got, ref, dtype, what, terms):
     that see no key are structural zeros, and a tensor that is mostly such zeros
     would otherwise have a diluted rms), floored at 2 % of the size of one term
     of its sums (`terms`).  Outside the support the result must be within the
-    same bound of zero.  With dO = 0 every gradient must be exactly zero."""
+    same bound of zero.  With dO = 0 every gradient must be exactly zero.
+    Returns {name: (mean error, largest excess over 2 u |ref|)} in units of u rms."""
     u = U[dtype]
+    stats = {}
     for name, g, r, term in zip(("dq", "dk", "dv"), got, ref, terms):
         assert np.all(np.isfinite(g)), f"{what} {name}: non-finite"
         if term == 0.0:
@@ -119,6 +121,9 @@ def compare(got, ref, dtype, what, terms):
             assert e.mean() <= MEAN_U * u * norm, f"{what} {name}: mean err {e.mean() / norm:.3e} rms"
         excess = err - REL_U * u * np.abs(r)
         assert excess.max() <= MAX_U * u * norm, f"{what} {name}: max err {excess.max() / norm:.3e} rms"
+        stats[name] = (float(err[sup].mean() / (u * norm)) if sup.any() else 0.0,
+                       float(excess.max() / (u * norm)))
+    return stats
 
 
 def check(q, k, v, do, causal, scale, what, dtype="bf16", fwd="oracle", exact=False):
@@ -126,7 +131,7 @@ def check(q, k, v, do, causal, scale, what, dtype="bf16", fwd="oracle", exact=Fa
     attn_bwd was given, or (exact=True) the exact gradient."""
     got, o_bits = gpu_grads(q, k, v, do, causal, scale, dtype=dtype, fwd=fwd, want_o=True)
     ref = oracle.attn_bwd(q, k, v, do, causal, scale, f16=dtype == "f16", o=None if exact else o_bits)
-    compare(got, ref, dtype, what, term_sizes(q, k, v, do, scale, dtype))
+    return compare(got, ref, dtype, what, term_sizes(q, k, v, do, scale, dtype))
 
 
 CASES = [
@@ -251,7 +256,9 @@ def test_bwd_headline_shape_every_element():
     kernels given the oracle's O (correctly rounded) and LSE."""
     B, S, H, D = 4, 4096, 16, 128
     q, k, v, do = problem(B, S, S, H, H, D, seed=90)
-    check(q, k, v, do, 1, 1 / math.sqrt(D), "headline every element")
+    stats = check(q, k, v, do, 1, 1 / math.sqrt(D), "headline every element")
+    print("headline every element, (mean, max excess) in u rms:",
+          {k_: (round(a, 3), round(b, 2)) for k_, (a, b) in stats.items()})
 
 
 def test_bwd_gqa_sampled():
