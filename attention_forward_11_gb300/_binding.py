@@ -24,7 +24,8 @@ _LIB_NAME = "libattn.so"
 # Every symbol include/attn.h declares (checked by the CPU tests).
 EXPORTED = ("attn_fwd", "attn_fwd_ex", "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_size",
             "attn_fwd_splitkv_noalloc", "attn_status_str", "attn_check_device_status",
-            "attn_kernel_launches", "attn_debug_wait_timeout", "attn_bwd", "attn_bwd_workspace_size")
+            "attn_kernel_launches", "attn_debug_wait_timeout", "attn_bwd", "attn_bwd_workspace_size",
+            "attn_debug_unit_rates")
 
 _lock = threading.Lock()
 _lib = None
@@ -69,6 +70,8 @@ def load_library():
         lib.attn_kernel_launches.restype = ctypes.c_ulonglong
         lib.attn_debug_wait_timeout.argtypes = [ctypes.c_uint, P]
         lib.attn_debug_wait_timeout.restype = I
+        lib.attn_debug_unit_rates.argtypes = [ctypes.POINTER(ctypes.c_double), I, P]
+        lib.attn_debug_unit_rates.restype = I
         lib.attn_fwd_splitkv_workspace_size.argtypes = [I, I, I, I, I, I, I,
                                                         ctypes.POINTER(ctypes.c_size_t)]
         lib.attn_fwd_splitkv_workspace_size.restype = I
@@ -280,3 +283,19 @@ def attn_kernel_launches() -> int:
 def attn_debug_wait_timeout(poll_limit: int, stream=None) -> int:
     """Launch the bounded-wait self-test kernel (an mbarrier nothing arrives on)."""
     return int(load_library().attn_debug_wait_timeout(int(poll_limit), _stream_handle(stream)))
+
+
+ATTN_UNIT_RATES = 8
+UNIT_RATE_NAMES = ("mma_ss_n128", "mma_ts_n128", "mma_ss_n256", "mma_ss_n64", "mma_ts_n64",
+                   "ex2_cycles_per_warp_instr", "ex2_per_cycle_per_sm", "sms")
+
+
+def attn_debug_unit_rates(stream=None) -> dict:
+    """Measured issue rates (diagnostic): SM clock cycles per tcgen05 MMA
+    (M = 128, K = 16) for the operand sources and N the kernels use, cycles per
+    warp-wide ex2 on one SM sub-partition, ex2 per cycle per SM, SMs measured."""
+    out = (ctypes.c_double * ATTN_UNIT_RATES)()
+    st = load_library().attn_debug_unit_rates(out, ATTN_UNIT_RATES, _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_debug_unit_rates")
+    return dict(zip(UNIT_RATE_NAMES, list(out)))

@@ -20,6 +20,7 @@
 #include "fmha_bwd_sm103.cuh"
 #include "fmha_fwd_d256_sm103.cuh"
 #include "fmha_fwd_sm103.cuh"
+#include "unit_rates_sm103.cuh"
 
 namespace {
 
@@ -671,4 +672,61 @@ extern "C" attn_status_t attn_debug_wait_timeout(unsigned int poll_limit, cudaSt
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return ATTN_OK;
+}
+
+// ---- measured unit rates (diagnostic)
+namespace {
+template <int kMode>
+attn_status_t run_mma_rate(int sms, cudaStream_t stream, double* clocks_per_mma) {
+    auto kern = attn::rates::mma_rate_kernel<kMode>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, attn::rates::kMmaSmem) !=
+        cudaSuccess)
+        return ATTN_ERR_CUDA;
+    kern<<<sms, 128, attn::rates::kMmaSmem, stream>>>();
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    long long c[attn::rates::kMaxSms];
+    if (cudaMemcpyFromSymbolAsync(c, attn::rates::g_rate_clocks, sizeof(long long) * sms, 0,
+                                  cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    double mean = 0.0;
+    for (int i = 0; i < sms; ++i) mean += static_cast<double>(c[i]);
+    *clocks_per_mma = mean / sms / (8.0 * attn::rates::kMmaIters);
+    return ATTN_OK;
+}
+}  // namespace
+
+extern "C" attn_status_t attn_debug_unit_rates(double* out, int n, cudaStream_t stream) {
+    if (out == nullptr || n < ATTN_UNIT_RATES) return ATTN_ERR_INVALID_ARG;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    if (sms < 1 || sms > attn::rates::kMaxSms) return ATTN_ERR_UNSUPPORTED;
+    attn_status_t st;
+    if ((st = run_mma_rate<0>(sms, stream, &out[0])) != ATTN_OK) return st;
+    if ((st = run_mma_rate<1>(sms, stream, &out[1])) != ATTN_OK) return st;
+    if ((st = run_mma_rate<2>(sms, stream, &out[2])) != ATTN_OK) return st;
+    if ((st = run_mma_rate<3>(sms, stream, &out[3])) != ATTN_OK) return st;
+    if ((st = run_mma_rate<4>(sms, stream, &out[4])) != ATTN_OK) return st;
+    attn::rates::ex2_rate_kernel<<<sms, attn::rates::kEx2Threads, 0, stream>>>(0.01f);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    long long c[attn::rates::kMaxSms];
+    if (cudaMemcpyFromSymbolAsync(c, attn::rates::g_rate_clocks, sizeof(long long) * sms,
+                                  sizeof(long long) * attn::rates::kMaxSms, cudaMemcpyDeviceToHost,
+                                  stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    double mean = 0.0;
+    for (int i = 0; i < sms; ++i) mean += static_cast<double>(c[i]);
+    mean /= sms;
+    // warp-level ex2 instructions per SM sub-partition: its warps x iterations x chains
+    const double per_smsp = (attn::rates::kEx2Threads / 32 / 4) * static_cast<double>(attn::rates::kEx2Iters) *
+                            attn::rates::kEx2Chains;
+    out[5] = mean / per_smsp;
+    out[6] = 4.0 * 32.0 / out[5];
+    out[7] = static_cast<double>(sms);
+    return attn_check_device_status(stream);
 }

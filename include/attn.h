@@ -198,6 +198,29 @@ unsigned long long attn_kernel_launches(void);
  */
 attn_status_t attn_debug_wait_timeout(unsigned int poll_limit, cudaStream_t stream);
 
+/*
+ * Measured issue rates of the units the attention loop leans on (diagnostic;
+ * no page defines it: it checks the design's assumption that the forward's
+ * 16384 exponentials per 128x128 tile fit under its 2 x 8 tensor-core products,
+ * so that no exponential has to move to the FMA pipe).  Runs one CTA per SM of
+ * the current device on `stream` and synchronises it.  out (host, n >=
+ * ATTN_UNIT_RATES doubles) receives:
+ *   out[0..4]  SM clock cycles per tcgen05.mma kind::f16 with M = 128, K = 16,
+ *              bf16 operands, fp32 accumulator, issued back to back by one
+ *              thread: [0] both operands in shared memory, N = 128; [1] A in
+ *              tensor memory, N = 128; [2] shared memory, N = 256; [3] shared
+ *              memory, N = 64; [4] A in tensor memory, N = 64
+ *   out[5]     cycles per warp-wide ex2.approx.ftz.f32 on one SM sub-partition
+ *              (two warps of independent exponentials per sub-partition)
+ *   out[6]     exponentials per cycle per SM (= 4 x 32 / out[5])
+ *   out[7]     number of SMs measured
+ * Returns ATTN_ERR_INVALID_ARG for a NULL `out` or n < ATTN_UNIT_RATES,
+ * ATTN_ERR_CUDA on a launch or copy failure, ATTN_ERR_TIMEOUT if the MMA
+ * completion wait ran out.
+ */
+#define ATTN_UNIT_RATES 8
+attn_status_t attn_debug_unit_rates(double* out, int n, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

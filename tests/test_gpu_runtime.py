@@ -52,3 +52,21 @@ def test_bad_tensors_raise_without_launch():
         fa.attn_fwd(mis, k, k)
     assert e.value.status == fa.ATTN_ERR_INVALID_ARG
     assert fa.attn_kernel_launches() == before
+
+
+def test_unit_rates():
+    """The measured rates the design rests on: a 128x128x16 MMA at 64 cycles from
+    either operand source, N = 256 twice that, N = 64 slower than half (the
+    tensor core is not fed faster at N = 64), and an exponential unit fast enough
+    that one 128x128 tile's 16384 exponentials take fewer cycles than its
+    sixteen 128x128x16 products (no exponential needs to move to the FMA pipe)."""
+    r = fa.attn_debug_unit_rates()
+    print("unit rates:", {k: round(v, 2) for k, v in r.items()})
+    assert fa.attn_check_device_status() == fa.ATTN_OK
+    assert r["sms"] >= 1
+    for key in ("mma_ss_n128", "mma_ts_n128"):
+        assert 56.0 <= r[key] <= 96.0, (key, r[key])
+    assert 1.7 <= r["mma_ss_n256"] / r["mma_ss_n128"] <= 2.3
+    assert r["mma_ss_n64"] > 0.5 * r["mma_ss_n128"]
+    assert r["ex2_per_cycle_per_sm"] > 0.0
+    assert 16384.0 / r["ex2_per_cycle_per_sm"] < 16.0 * r["mma_ss_n128"]

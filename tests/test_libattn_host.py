@@ -186,3 +186,10 @@ def test_bwd_workspace_size(lib):
     with pytest.raises(fa.AttnError) as e:  # the forward takes D = 256, the backward does not
         fa.attn_bwd_workspace_size(1, 256, 256, 2, 2, 256)
     assert e.value.status == fa.ATTN_ERR_UNSUPPORTED
+
+
+def test_unit_rates_arguments_checked_before_any_launch(lib):
+    import ctypes
+    out = (ctypes.c_double * 8)()
+    assert lib.attn_debug_unit_rates(None, 8, None) == fa.ATTN_ERR_INVALID_ARG
+    assert lib.attn_debug_unit_rates(out, 7, None) == fa.ATTN_ERR_INVALID_ARG
