@@ -18,7 +18,11 @@
 //                next unit, so the store never sits on the softmax critical path.
 //   warp  12     MMA issuer (one elected lane): S_t = Q_t K^T and O_t += P_t V
 //   warp  13     TMA producer (one thread): Q of each unit (plus an L2 prefetch of
-//                the next unit's Q), K and V tiles through two shared-memory rings
+//                the next unit's Q), K and V tiles in stages: stage g carries V of
+//                KV tile g-1 and K of KV tile g (tiles numbered across units), so the
+//                MMA warp waits once per KV step, for both operands of that step
+//                (P.V with V_j, then S_{j+1} with K_{j+1}), and releases both with
+//                one commit
 //   warps 14-15  idle
 // Registers are split with setmaxnreg: softmax 176, epilogue 88, MMA/producer 72
 // per thread (2*176 + 88 + 72 = 4 * 128, the launch allocation of 128 per thread).
@@ -54,20 +58,13 @@
 
 #include "sm103_ptx.cuh"
 
-#ifndef ATTN_KSTAGES
-#define ATTN_KSTAGES 2
-#endif
-#ifndef ATTN_VSTAGES
-#define ATTN_VSTAGES 2
-#endif
 
 namespace attn {
 
 constexpr int kBM = 128;                 // query rows per tile (= TMEM lanes)
 constexpr int kBN = 128;                 // keys per KV tile
 constexpr int kTiles = 2;                // query tiles per unit
-constexpr int kKStages = ATTN_KSTAGES;   // K ring depth
-constexpr int kVStages = ATTN_VSTAGES;   // V ring depth
+constexpr int kStages = 2;              // K/V stages in flight (one K slot and one V slot each)
 constexpr int kHalfBytes = kBM * 64 * 2;         // 128 rows x one 64-column, 128-byte-swizzled half
 constexpr int kSoftmaxWarps = 4 * kTiles;          // warpgroups 0 and 1
 constexpr int kEpilogueWarp0 = kSoftmaxWarps;      // warpgroup 2
@@ -85,11 +82,9 @@ constexpr float kRescaleLog2 = 8.0f;     // raise the running max only past 2^8
 enum : int {
     BAR_QFULL = 0,
     BAR_QEMPTY = BAR_QFULL + kTiles,
-    BAR_KFULL = BAR_QEMPTY + kTiles,
-    BAR_KEMPTY = BAR_KFULL + kKStages,
-    BAR_VFULL = BAR_KEMPTY + kKStages,
-    BAR_VEMPTY = BAR_VFULL + kVStages,
-    BAR_SFULL = BAR_VEMPTY + kVStages,
+    BAR_KVFULL = BAR_QEMPTY + kTiles,        // [stage]: V_{g-1} and K_g landed
+    BAR_KVEMPTY = BAR_KVFULL + kStages,      // [stage]: both read by their last MMA
+    BAR_SFULL = BAR_KVEMPTY + kStages,
     BAR_PFULL = BAR_SFULL + kTiles,          // [tile][half]: P of 64 keys in TMEM
     BAR_ODONE = BAR_PFULL + 2 * kTiles,
     BAR_OFREE = BAR_ODONE + kTiles,
@@ -108,8 +103,8 @@ struct Geo {
     static constexpr int kTileBytes = kBM * kD * 2;  // Q, K or V tile
     static constexpr int kSmemQ = 0;
     static constexpr int kSmemK = kSmemQ + kTiles * kTileBytes;
-    static constexpr int kSmemV = kSmemK + kKStages * kTileBytes;
-    static constexpr int kSmemStage = kSmemV + kVStages * kTileBytes;  // O staging: one half
+    static constexpr int kSmemV = kSmemK + kStages * kTileBytes;
+    static constexpr int kSmemStage = kSmemV + kStages * kTileBytes;  // O staging: one half
     static constexpr int kSmemStats = kSmemStage + kHalfBytes;         // per tile and row: (m, l)
     static constexpr int kSmemBar = kSmemStats + kTiles * kBM * 8;
     static constexpr int kSmemTmemSlot = kSmemBar + BAR_COUNT * 8;
@@ -318,13 +313,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(BAR_STATSFULL + t), 4 * 32);
             mbar_init(bar(BAR_STATSFREE + t), 4 * 32);
         }
-        for (int s = 0; s < kKStages; ++s) {
-            mbar_init(bar(BAR_KFULL + s), 1);
-            mbar_init(bar(BAR_KEMPTY + s), 1);
-        }
-        for (int s = 0; s < kVStages; ++s) {
-            mbar_init(bar(BAR_VFULL + s), 1);
-            mbar_init(bar(BAR_VEMPTY + s), 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar(BAR_KVFULL + s), 1);
+            mbar_init(bar(BAR_KVEMPTY + s), 1);
         }
         mbar_init(bar(BAR_MMADONE), 1);
         *abort_flag = 0;
@@ -350,66 +341,93 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (warp == kLoadWarp) {
         // =========================== TMA producer ===========================
         if (lane == 0) {
+            // K and V stream as stages: stage g holds V of fill g-1 and K of fill g
+            // (fills numbered across units), both released by the same MMA commit
+            // (the end of the KV step that reads V_{g-1} with P.V and K_g with the
+            // next S); barrier pair KVFULL/KVEMPTY[g % kStages].  The Q tiles of a
+            // unit are loaded right after the stage that brings its K_0.
             const uint64_t pol_q = l2_policy_evict_first();
             const uint64_t pol_kv = l2_policy_evict_last();
-            int k_issued = 0, v_issued = 0;  // KV ring fills issued so far
+            int g = 0;                       // stages issued
             int q_issued[kTiles] = {0, 0};   // Q_t fills issued so far
+            int jq = 0;                      // next unit whose Q is to be loaded
             bool ok = true;
-            for (int j = 0; ok; ++j) {
-                Unit w;
-                if (!get_work(p, sched, j, w)) break;
-                for (int t = 0; t < kTiles; ++t) {
-                    // Q_t of the previous unit must be consumed by its last S_t MMA
-                    if (j > 0 && !wait_bounded(bar(BAR_QEMPTY + t), (j - 1) & 1, abort_flag, limit)) {
-                        ok = false;
-                        break;
+            auto issue_q_upto = [&](int jmax) -> bool {
+                for (; jq <= jmax; ++jq) {
+                    Unit w;
+                    if (!get_work(p, sched, jq, w)) return true;
+                    for (int t = 0; t < kTiles; ++t) {
+                        if (jq > 0 && !wait_bounded(bar(BAR_QEMPTY + t), (jq - 1) & 1, abort_flag, limit))
+                            return false;
+                        mbar_arrive_expect_tx(bar(BAR_QFULL + t), G::kTileBytes);
+                        for (int h = 0; h < G::kHalves; ++h)
+                            tma_load_4d(sbase + G::kSmemQ + t * G::kTileBytes + h * kHalfBytes, &tm_q, h * 64,
+                                        w.hq(t), w.row(t), w.b, bar(BAR_QFULL + t), pol_q);
+                        ++q_issued[t];
                     }
-                    mbar_arrive_expect_tx(bar(BAR_QFULL + t), G::kTileBytes);
-                    for (int h = 0; h < G::kHalves; ++h)
-                        tma_load_4d(sbase + G::kSmemQ + t * G::kTileBytes + h * kHalfBytes, &tm_q, h * 64,
-                                    w.hq(t), w.row(t), w.b, bar(BAR_QFULL + t), pol_q);
-                    ++q_issued[t];
+                    Unit wn;
+                    if (get_work(p, sched, jq + 1, wn)) {  // warm L2 with the next unit's Q meanwhile
+                        for (int t = 0; t < kTiles; ++t)
+                            for (int h = 0; h < G::kHalves; ++h)
+                                tma_prefetch_l2_4d(&tm_q, h * 64, wn.hq(t), wn.row(t), wn.b);
+                    }
                 }
-                if (!ok) break;
-                Unit wn;
-                if (get_work(p, sched, j + 1, wn)) {  // warm L2 with the next unit's Q meanwhile
-                    for (int t = 0; t < kTiles; ++t)
-                        for (int h = 0; h < G::kHalves; ++h) tma_prefetch_l2_4d(&tm_q, h * 64, wn.hq(t), wn.row(t), wn.b);
+                return true;
+            };
+            // K cursor (the fill of the next stage's K) and V cursor (the previous one)
+            int jk = 0, ktk = 0;
+            Unit wk;
+            bool have_k = get_work(p, sched, 0, wk);
+            while (have_k && ktk >= wk.nmax()) {
+                ++jk;
+                ktk = 0;
+                have_k = get_work(p, sched, jk, wk);
+            }
+            Unit wv = wk;
+            int ktv = 0;
+            bool have_v = false;
+            while (ok && (have_k || have_v)) {
+                const int st = g % kStages, use = g / kStages;
+                if (use > 0 && !wait_bounded(bar(BAR_KVEMPTY + st), (use - 1) & 1, abort_flag, limit)) {
+                    ok = false;
+                    break;
                 }
-                const int nm = w.nmax();
-                for (int kt = 0; kt < nm; ++kt) {
-                    const int ks = k_issued % kKStages, kuse = k_issued / kKStages;
-                    if (kuse > 0 && !wait_bounded(bar(BAR_KEMPTY + ks), (kuse - 1) & 1, abort_flag, limit)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(bar(BAR_KFULL + ks), G::kTileBytes);
-                    for (int h = 0; h < G::kHalves; ++h)
-                        tma_load_4d(sbase + G::kSmemK + ks * G::kTileBytes + h * kHalfBytes, &tm_k, h * 64,
-                                    w.hkv, (w.kb + kt) * kBN, w.b, bar(BAR_KFULL + ks), pol_kv);
-                    ++k_issued;
-                    const int vs = v_issued % kVStages, vuse = v_issued / kVStages;
-                    if (vuse > 0 && !wait_bounded(bar(BAR_VEMPTY + vs), (vuse - 1) & 1, abort_flag, limit)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(bar(BAR_VFULL + vs), G::kTileBytes);
+                mbar_arrive_expect_tx(bar(BAR_KVFULL + st), ((have_k ? 1 : 0) + (have_v ? 1 : 0)) * G::kTileBytes);
+                if (have_v) {
+                    const int vs = (g - 1) % kStages;
                     for (int h = 0; h < G::kHalves; ++h)
                         tma_load_4d(sbase + G::kSmemV + vs * G::kTileBytes + h * kHalfBytes, &tm_v, h * 64,
-                                    w.hkv, (w.kb + kt) * kBN, w.b, bar(BAR_VFULL + vs), pol_kv);
-                    ++v_issued;
+                                    wv.hkv, (wv.kb + ktv) * kBN, wv.b, bar(BAR_KVFULL + st), pol_kv);
+                }
+                if (have_k) {
+                    for (int h = 0; h < G::kHalves; ++h)
+                        tma_load_4d(sbase + G::kSmemK + st * G::kTileBytes + h * kHalfBytes, &tm_k, h * 64,
+                                    wk.hkv, (wk.kb + ktk) * kBN, wk.b, bar(BAR_KVFULL + st), pol_kv);
+                    if (ktk == 0 && !issue_q_upto(jk)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                ++g;
+                have_v = have_k;
+                wv = wk;
+                ktv = ktk;
+                if (have_k) {
+                    ++ktk;
+                    while (have_k && ktk >= wk.nmax()) {
+                        ++jk;
+                        ktk = 0;
+                        have_k = get_work(p, sched, jk, wk);
+                    }
                 }
             }
+            if (ok) issue_q_upto(0x7fffffff);  // units after the last fill (without KV work) still need Q
             // drain: every copy this thread issued has landed before the CTA may exit
             for (int t = 0; t < kTiles; ++t)
                 if (q_issued[t] > 0) drain_bounded(bar(BAR_QFULL + t), (q_issued[t] - 1) & 1, limit);
-            for (int s = 0; s < kKStages; ++s) {
-                const int fills = k_issued > s ? (k_issued - 1 - s) / kKStages + 1 : 0;
-                if (fills) drain_bounded(bar(BAR_KFULL + s), (fills - 1) & 1, limit);
-            }
-            for (int s = 0; s < kVStages; ++s) {
-                const int fills = v_issued > s ? (v_issued - 1 - s) / kVStages + 1 : 0;
-                if (fills) drain_bounded(bar(BAR_VFULL + s), (fills - 1) & 1, limit);
+            for (int st = 0; st < kStages; ++st) {
+                const int fills = g > st ? (g - 1 - st) / kStages + 1 : 0;
+                if (fills) drain_bounded(bar(BAR_KVFULL + st), (fills - 1) & 1, limit);
             }
         }
         __syncwarp();
@@ -445,27 +463,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                             (accumulate || kk > 0) ? 1u : 0u);
             }
         };
-        int kv = 0;                 // KV tiles consumed so far (ring position)
+        int kv = 0;                 // KV tiles consumed so far (stage kv carries K_kv)
         int sc0 = 0, sc1 = 0;       // S_t products issued so far (s_full / p_full phase)
         bool ok = true;
         for (int j = 0; ok; ++j) {
             Unit w;
             if (!get_work(p, sched, j, w)) break;
             const int nm = w.nmax();
-            // S_t(0) for each tile that has work; Q_t must have landed
+            // S_t(0) for each tile that has work; Q_t must have landed, and stage kv
+            // (this unit's K_0, with V of the previous unit's last KV tile)
             bool k_ready = false;
             for (int t = 0; t < kTiles && ok; ++t) {
                 ok = wait_bounded(bar(BAR_QFULL + t), j & 1, abort_flag, limit);
                 if (!ok) break;
                 if (w.n(t) > 0 && !k_ready) {
-                    ok = wait_bounded(bar(BAR_KFULL + kv % kKStages), (kv / kKStages) & 1, abort_flag, limit);
+                    ok = wait_bounded(bar(BAR_KVFULL + kv % kStages), (kv / kStages) & 1, abort_flag, limit);
                     if (!ok) break;
                     k_ready = true;
                 }
                 tc_fence_after();
                 if (elect_one()) {
                     if (w.n(t) > 0) {
-                        issue_qk(t, kv % kKStages);
+                        issue_qk(t, kv % kStages);
                         mma_commit(bar(BAR_SFULL + t));
                     }
                     if (w.n(t) <= 1) mma_commit(bar(BAR_QEMPTY + t));  // Q_t no longer read
@@ -476,18 +495,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (!ok) break;
-            if (nm > 0) {
-                if (elect_one()) mma_commit(bar(BAR_KEMPTY + kv % kKStages));
+            if (nm > 0) {  // stage kv: its V was read by the previous unit's last P.V, its K now
+                if (elect_one()) mma_commit(bar(BAR_KVEMPTY + kv % kStages));
                 __syncwarp();
             }
             for (int kt = 0; ok && kt < nm; ++kt) {
-                const int vs = kv % kVStages, vuse = kv / kVStages;
-                const int kn = kv + 1;  // ring position of K_{kt+1}
-                if (!wait_bounded(bar(BAR_VFULL + vs), vuse & 1, abort_flag, limit)) {
+                const int vs = kv % kStages;
+                const int kn = kv + 1;  // stage kn: V_{kt} and K_{kt+1} (or the next unit's K_0)
+                if (!wait_bounded(bar(BAR_KVFULL + kn % kStages), (kn / kStages) & 1, abort_flag, limit)) {
                     ok = false;
                     break;
                 }
-                bool kn_ready = false;
+                tc_fence_after();
                 for (int t = 0; t < kTiles; ++t) {
                     const int nt = w.n(t);
                     if (kt < nt) {
@@ -526,17 +545,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         __syncwarp();
                     }
                     if (kt + 1 < nt) {
-                        if (!kn_ready) {
-                            if (!wait_bounded(bar(BAR_KFULL + kn % kKStages), (kn / kKStages) & 1, abort_flag,
-                                              limit)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                            kn_ready = true;
-                        }
                         if (elect_one()) {
-                            issue_qk(t, kn % kKStages);
+                            issue_qk(t, kn % kStages);
                             mma_commit(bar(BAR_SFULL + t));
                             if (kt + 2 == nt) mma_commit(bar(BAR_QEMPTY + t));  // last S_t of the unit
                         }
@@ -545,10 +555,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (!ok) break;
-                if (elect_one()) {
-                    mma_commit(bar(BAR_VEMPTY + vs));
-                    if (kt + 1 < nm) mma_commit(bar(BAR_KEMPTY + kn % kKStages));
-                }
+                // stage kn is free once V_kt and K_{kt+1} have been read; after the unit's
+                // last step its K belongs to the next unit and is released there
+                if (kt + 1 < nm && elect_one()) mma_commit(bar(BAR_KVEMPTY + kn % kStages));
                 __syncwarp();
                 ++kv;
             }
