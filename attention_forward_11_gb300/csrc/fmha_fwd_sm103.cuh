@@ -403,12 +403,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int h = 0; h < G::kHalves; ++h)
                         tma_load_4d(sbase + G::kSmemK + st * G::kTileBytes + h * kHalfBytes, &tm_k, h * 64,
                                     wk.hkv, (wk.kb + ktk) * kBN, wk.b, bar(BAR_KVFULL + st), pol_kv);
-                    if (ktk == 0 && !issue_q_upto(jk)) {
-                        ok = false;
-                        break;
-                    }
                 }
-                ++g;
+                ++g;  // counted before anything can fail: the drain below waits for these copies
+                if (have_k && ktk == 0 && !issue_q_upto(jk)) {
+                    ok = false;
+                    break;
+                }
                 have_v = have_k;
                 wv = wk;
                 ktv = ktk;
