@@ -1,7 +1,6 @@
 """Host-side pieces of the benchmark harness (no GPU): the FLOP counts behind
 `value` and `roofline.achieved`, the digest gate on the committed DRAM
 traffic, and the clock sampler's reason decoding (NVML replaced by a fake)."""
-import ctypes
 import importlib.util
 import json
 import os
