@@ -180,7 +180,7 @@ __host__ __device__ __forceinline__ int kv_tiles_for_rows(const BwdParams& p, in
 // warp's loads of O and dO are contiguous: each lane loads 16 bytes of each,
 // kD / 8 lanes cover a row, and a warp handles kPrepIters groups of
 // 32 / (kD / 8) rows with all loads issued before the reductions.
-constexpr int kPrepIters = 4;
+constexpr int kPrepIters = 2;
 template <int kD>
 __host__ __device__ constexpr int prep_rows_per_warp() {
     return (32 / (kD / 8)) * kPrepIters;
