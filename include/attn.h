@@ -214,9 +214,11 @@ attn_status_t attn_debug_wait_timeout(unsigned int poll_limit, cudaStream_t stre
  *              (two warps of independent exponentials per sub-partition)
  *   out[6]     exponentials per cycle per SM (= 4 x 32 / out[5])
  *   out[7]     number of SMs measured
- * Returns ATTN_ERR_INVALID_ARG for a NULL `out` or n < ATTN_UNIT_RATES,
- * ATTN_ERR_CUDA on a launch or copy failure, ATTN_ERR_TIMEOUT if the MMA
- * completion wait ran out.
+ * Returns ATTN_ERR_INVALID_ARG for a NULL `out` or n < ATTN_UNIT_RATES (nothing
+ * is launched), ATTN_ERR_CUDA on a launch or copy failure, and otherwise the
+ * result of attn_check_device_status(stream): ATTN_ERR_TIMEOUT if the MMA
+ * completion wait ran out, or if any earlier libattn kernel's bounded wait had
+ * (the device status word is read and cleared, as that call does).
  */
 #define ATTN_UNIT_RATES 8
 attn_status_t attn_debug_unit_rates(double* out, int n, cudaStream_t stream);
