@@ -23,7 +23,8 @@ _LIB_NAME = "libattn.so"
 
 # Every symbol include/attn.h declares (checked by the CPU tests).
 EXPORTED = ("attn_fwd", "attn_fwd_ex", "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_size",
-            "attn_fwd_splitkv_noalloc", "attn_status_str", "attn_check_device_status",
+            "attn_fwd_splitkv_noalloc", "attn_status_str", "attn_last_device_status",
+            "attn_check_device_status",
             "attn_kernel_launches", "attn_debug_wait_timeout", "attn_bwd", "attn_bwd_workspace_size",
             "attn_debug_unit_rates")
 
@@ -66,6 +67,8 @@ def load_library():
         lib.attn_status_str.restype = ctypes.c_char_p
         lib.attn_check_device_status.argtypes = [P]
         lib.attn_check_device_status.restype = I
+        lib.attn_last_device_status.argtypes = []
+        lib.attn_last_device_status.restype = I
         lib.attn_kernel_launches.argtypes = []
         lib.attn_kernel_launches.restype = ctypes.c_ulonglong
         lib.attn_debug_wait_timeout.argtypes = [ctypes.c_uint, P]
@@ -268,6 +271,12 @@ def attn_bwd(q, k, v, o, lse, do, causal: int = 0, scale: float | None = None, d
     if st != ATTN_OK:
         raise AttnError(st, "attn_bwd")
     return dq, dk, dv
+
+
+def attn_last_device_status() -> int:
+    """Wait for all work on the current device, then return (and clear) the
+    kernels' device status word."""
+    return int(load_library().attn_last_device_status())
 
 
 def attn_check_device_status(stream=None) -> int:

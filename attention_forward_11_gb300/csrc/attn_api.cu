@@ -12,7 +12,6 @@
 #include <cstring>
 #include <memory>
 #include <mutex>
-#include <vector>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -132,8 +131,9 @@ attn_status_t check_pointers(const void* q, const void* k, const void* v, const 
     if (ranges_overlap(o, q_bytes, q, q_bytes) || ranges_overlap(o, q_bytes, k, kv_bytes) ||
         ranges_overlap(o, q_bytes, v, kv_bytes))
         return ATTN_ERR_INVALID_ARG;
-    if (lse && (ranges_overlap(lse, (size_t)B * Hq * Sq * 4, o, q_bytes) ||
-                ranges_overlap(lse, (size_t)B * Hq * Sq * 4, q, q_bytes)))
+    const size_t lse_bytes = (size_t)B * Hq * Sq * 4;
+    if (lse && (ranges_overlap(lse, lse_bytes, o, q_bytes) || ranges_overlap(lse, lse_bytes, q, q_bytes) ||
+                ranges_overlap(lse, lse_bytes, k, kv_bytes) || ranges_overlap(lse, lse_bytes, v, kv_bytes)))
         return ATTN_ERR_INVALID_ARG;
     return ATTN_OK;
 }
@@ -194,11 +194,19 @@ size_t workspace_bytes_for(int n_slots, int D) {
     return o_pad + ml_bytes;
 }
 
+// The split plan: the (unit, KV tile) iterations, units in the plain schedule's
+// order, cut into G = min(#SMs, total) equal contiguous shares, one per CTA; a
+// unit that straddles shares becomes one piece per share, each with a workspace
+// slot, merged afterwards by the combine kernel.  Fixed-size storage only (no
+// heap), so every split-KV entry point, the no-allocation one included, runs
+// this one planner.
 void build_split_plan(const attn::FwdParams& p, int sms, SplitPlan* plan) {
     plan->split = false;
     if (p.D == 256) return;  // head size 256 runs its own one-tile-per-CTA kernel, unsplit
     if (p.n_units < 1 || p.n_units > attn::kMaxPieces) return;
-    std::vector<int> W(p.n_units);
+    int W[attn::kMaxPieces];
+    long long bnd[attn::kMaxSplitCtas + 1];
+    unsigned short piece_cta[attn::kMaxPieces];
     long long T = 0;
     for (int u = 0; u < p.n_units; ++u) {
         W[u] = attn::decode_unit(p, u).nmax();
@@ -207,26 +215,23 @@ void build_split_plan(const attn::FwdParams& p, int sms, SplitPlan* plan) {
     }
     const int G = static_cast<int>(std::min<long long>(std::min(sms, attn::kMaxSplitCtas), T));
     if (G < 1) return;
-    std::vector<long long> bnd(G + 1);
     for (int c = 0; c <= G; ++c) bnd[c] = (long long)c * T / G;
     attn::SplitSched& sc = plan->sched;
     attn::CombineTable& cb = plan->comb;
-    std::vector<int> piece_cta;
     int n_pieces = 0, n_slots = 0, n_comb = 0, c = 0;
     long long off = 0;
     auto add = [&](int u, int kb, int ke, int slot, int cta) -> bool {
         if (n_pieces >= attn::kMaxPieces) return false;
         sc.piece[n_pieces] = attn::Piece{u, static_cast<unsigned int>(kb) | (static_cast<unsigned int>(ke) << 16),
                                          slot};
-        piece_cta.push_back(cta);
-        ++n_pieces;
+        piece_cta[n_pieces++] = static_cast<unsigned short>(cta);
         return true;
     };
     for (int u = 0; u < p.n_units; ++u) {
         const long long a = off, e = off + W[u];
         while (c < G - 1 && a >= bnd[c + 1]) ++c;
-        if (W[u] == 0) {  // no KV tile at all: still writes O = 0, LSE = -inf
-            if (!add(u, 0, 0, -1, c)) return;
+        if (W[u] == 0) {
+            if (!add(u, 0, 0, -1, c)) return;  // no KV tile at all: still writes O = 0, LSE = -inf
             continue;
         }
         int c1 = c;
@@ -428,68 +433,6 @@ void* static_scratch_address(int dev) {
     return addr[dev];
 }
 
-// The split plan of build_split_plan, computed in fixed-size storage (no heap).
-void build_split_plan_fixed(const attn::FwdParams& p, int sms, SplitPlan* plan) {
-    plan->split = false;
-    if (p.D == 256) return;  // as build_split_plan
-    if (p.n_units < 1 || p.n_units > attn::kMaxPieces) return;
-    int W[attn::kMaxPieces];
-    long long bnd[attn::kMaxSplitCtas + 1];
-    unsigned short piece_cta[attn::kMaxPieces];
-    long long T = 0;
-    for (int u = 0; u < p.n_units; ++u) {
-        W[u] = attn::decode_unit(p, u).nmax();
-        if (W[u] > 0xFFFF) return;
-        T += W[u];
-    }
-    const int G = static_cast<int>(std::min<long long>(std::min(sms, attn::kMaxSplitCtas), T));
-    if (G < 1) return;
-    for (int c = 0; c <= G; ++c) bnd[c] = (long long)c * T / G;
-    attn::SplitSched& sc = plan->sched;
-    attn::CombineTable& cb = plan->comb;
-    int n_pieces = 0, n_slots = 0, n_comb = 0, c = 0;
-    long long off = 0;
-    auto add = [&](int u, int kb, int ke, int slot, int cta) -> bool {
-        if (n_pieces >= attn::kMaxPieces) return false;
-        sc.piece[n_pieces] = attn::Piece{u, static_cast<unsigned int>(kb) | (static_cast<unsigned int>(ke) << 16),
-                                         slot};
-        piece_cta[n_pieces++] = static_cast<unsigned short>(cta);
-        return true;
-    };
-    for (int u = 0; u < p.n_units; ++u) {
-        const long long a = off, e = off + W[u];
-        while (c < G - 1 && a >= bnd[c + 1]) ++c;
-        if (W[u] == 0) {
-            if (!add(u, 0, 0, -1, c)) return;
-            continue;
-        }
-        int c1 = c;
-        while (c1 < G - 1 && e > bnd[c1 + 1]) ++c1;
-        if (c1 == c) {
-            if (!add(u, 0, W[u], -1, c)) return;
-        } else {
-            if (n_comb >= attn::kMaxCombine) return;
-            cb.e[n_comb++] = attn::CombineEntry{u, n_slots, c1 - c + 1};
-            for (int cc = c; cc <= c1; ++cc) {
-                const long long kb = std::max(a, bnd[cc]) - a, ke = std::min(e, bnd[cc + 1]) - a;
-                if (!add(u, static_cast<int>(kb), static_cast<int>(ke), n_slots++, cc)) return;
-            }
-        }
-        off = e;
-    }
-    if (n_comb == 0) return;
-    int i = 0;
-    for (int cc = 0; cc <= G; ++cc) {
-        while (i < n_pieces && piece_cta[i] < cc) ++i;
-        sc.cta_begin[cc] = static_cast<unsigned short>(i);
-    }
-    sc.n_pieces = n_pieces;
-    cb.n = n_comb;
-    plan->grid = G;
-    plan->n_slots = n_slots;
-    plan->split = true;
-}
-
 }  // namespace
 
 extern "C" attn_status_t attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
@@ -512,7 +455,7 @@ extern "C" attn_status_t attn_fwd_splitkv_noalloc(const void* q, const void* k, 
     static std::mutex plan_mu;
     static SplitPlan plan;
     std::lock_guard<std::mutex> lock(plan_mu);
-    build_split_plan_fixed(p, sms, &plan);
+    build_split_plan(p, sms, &plan);
     if (plan.split && workspace_bytes_for(plan.n_slots, D) > kStaticScratchBytes) return ATTN_ERR_UNSUPPORTED;
     CUtensorMap tm[4];
     if (!encode_maps(q, k, v, o, B, Sq, Skv, Hq, Hkv, D, tm)) return ATTN_ERR_CUDA;
@@ -649,8 +592,11 @@ extern "C" const char* attn_status_str(attn_status_t status) {
     return "ATTN_UNKNOWN_STATUS";
 }
 
-extern "C" attn_status_t attn_check_device_status(cudaStream_t stream) {
-    if (cudaStreamSynchronize(stream) != cudaSuccess) return ATTN_ERR_CUDA;
+namespace {
+
+// Reads and clears the current device's status word (the caller has synchronised
+// whatever work it wants covered).
+attn_status_t read_and_clear_status() {
     unsigned int word = 0;
     if (cudaMemcpyFromSymbol(&word, attn::g_attn_status, sizeof word) != cudaSuccess)
         return ATTN_ERR_CUDA;
@@ -660,6 +606,18 @@ extern "C" attn_status_t attn_check_device_status(cudaStream_t stream) {
             return ATTN_ERR_CUDA;
     }
     return (word & attn::kStatusTimeout) ? ATTN_ERR_TIMEOUT : ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" attn_status_t attn_check_device_status(cudaStream_t stream) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    return read_and_clear_status();
+}
+
+extern "C" attn_status_t attn_last_device_status(void) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
+    return read_and_clear_status();
 }
 
 extern "C" unsigned long long attn_kernel_launches(void) {
@@ -704,6 +662,9 @@ extern "C" attn_status_t attn_debug_unit_rates(double* out, int n, cudaStream_t 
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return ATTN_ERR_CUDA;
     if (sms < 1 || sms > attn::rates::kMaxSms) return ATTN_ERR_UNSUPPORTED;
+    // an earlier kernel's timeout is kept and reported, not wiped by this diagnostic
+    const attn_status_t earlier = attn_check_device_status(stream);
+    if (earlier == ATTN_ERR_CUDA) return earlier;
     attn_status_t st;
     if ((st = run_mma_rate<0>(sms, stream, &out[0])) != ATTN_OK) return st;
     if ((st = run_mma_rate<1>(sms, stream, &out[1])) != ATTN_OK) return st;
@@ -728,5 +689,6 @@ extern "C" attn_status_t attn_debug_unit_rates(double* out, int n, cudaStream_t 
     out[5] = mean / per_smsp;
     out[6] = 4.0 * 32.0 / out[5];
     out[7] = static_cast<double>(sms);
-    return attn_check_device_status(stream);
+    const attn_status_t now = attn_check_device_status(stream);
+    return now != ATTN_OK ? now : earlier;
 }

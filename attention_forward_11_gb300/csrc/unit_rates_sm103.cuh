@@ -54,6 +54,7 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel() {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    volatile int* mma_done = reinterpret_cast<volatile int*>(smem + 98304 + 12);
     constexpr bool kTS = kMode == 1 || kMode == 4;
     constexpr uint32_t kN = kMode == 2 ? 256 : (kMode == 3 || kMode == 4) ? 64 : 128;
     if (threadIdx.x == 0) {
@@ -75,12 +76,20 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel() {
         mma_commit(bar);
         bool done = false;
         for (unsigned int i = 0; i < kWaitLimit && !done; ++i) done = mbar_try_wait(bar, 0);
-        if (!done) atomicOr(&g_attn_status, kStatusTimeout);
         g_rate_clocks[blockIdx.x] = clock64() - t0;
+        if (!done) {
+            atomicOr(&g_attn_status, kStatusTimeout);
+            // a second bounded wait: the MMAs may still be reading shared memory
+            // and writing tensor memory, which must not be freed under them
+            for (unsigned int i = 0; i < kWaitLimit && !done; ++i) done = mbar_try_wait(bar, 0);
+        }
+        *mma_done = done ? 1 : 0;
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) {
+    // freed only when every MMA is known complete; otherwise the status word
+    // already reports the timeout and the columns are left to the CTA's exit
+    if (warp == 0 && *mma_done) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }

@@ -13,6 +13,15 @@ every step are inside its timed region, pipelined over two device buffer sets
 bf16 tensor peak.  `cpu_baseline` times the fp64 oracle on a bounded sample of
 the same workload on the host cores.
 
+The timed region is the K-step block repeated until it spans at least
+--min-timed-seconds (default 1 s), each block bracketed by a barrier and a
+device synchronisation, so the NVML sampler (every 5 ms) sees the kernel under
+load; `value` is the mean over every timed step.  `roofline.clock_matched`
+relates the kernel to the tensor pipe's rate at the SM clock sampled meanwhile
+(8192 bf16 FLOP per clock per SM: one 128x128x16 MMA every 64 cycles, the
+measured rate of this part).  `workloads` holds kernel-only timings of the
+other benchmark shapes (a few steps each, same rules).
+
 --path bwd times attn_bwd instead (one step = the gradients dq, dk, dv of one
 forward, 2.5x its FLOPs); it prints no cpu_baseline.
 
@@ -41,6 +50,11 @@ METRIC_BWD = "attention bwd TFLOP/s (2.5x the forward's FLOPs, causal halved)"
 UNIT = "TFLOP/s"
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 256 << 20
+# bf16 FLOP per SM clock of the tensor pipe: 2*128*128*16 per 64-cycle MMA (measured rate)
+TENSOR_FLOP_PER_CLK_PER_SM = 8192
+# shapes whose kernel-only throughput is reported beside the headline
+OTHER_WORKLOADS = ("tiny_causal", "tiny_noncausal", "gqa_causal_2x32x8_8192", "long_sharp_1x16x16384",
+                   "chunked_prefill_gqa_64x8_512x32768")
 
 
 def metric_flops(w) -> int:
@@ -201,6 +215,46 @@ def oracle_sample_rate(w, target_s: float, seed: int = 0, q=None, k=None, v=None
     return flops_of(rows) / dt / 1e12, dt, n, oracle.num_threads()
 
 
+def oracle_one_core(workload: str, target_s: float):
+    """The same oracle sample timed with one OpenMP thread, in a child process
+    (the thread count is fixed when the oracle library loads)."""
+    import subprocess
+    code = ("import json, sys; sys.path.insert(0, %r); import bench; "
+            "from attention_forward_11_gb300 import inputs; "
+            "w = inputs.WORKLOADS[%r]; tf, dt, n, c = bench.oracle_sample_rate(w, %r); "
+            "print(json.dumps([tf, dt, n, c]))") % (ROOT, workload, target_s)
+    env = {**os.environ, "OMP_NUM_THREADS": "1"}
+    out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                         check=True, timeout=600)
+    tf, dt, n, cores = json.loads(out.stdout.strip().splitlines()[-1])
+    return tf, dt, n, cores
+
+
+def numpy_fp64_rate(w, seed: int = 0):
+    """numpy fp64 (BLAS matmuls) on one (batch, head) slice of the workload: the
+    plain masked softmax(scale Q K^T) V, timed; returns (TFLOP/s, seconds)."""
+    import numpy as np
+    from attention_forward_11_gb300 import inputs
+    q = inputs.normal_bf16((w.Sq, w.D), w.q_sigma, seed, 0).astype(np.uint32) << 16
+    k = inputs.normal_bf16((w.Skv, w.D), w.kv_sigma, seed, 1).astype(np.uint32) << 16
+    v = inputs.normal_bf16((w.Skv, w.D), w.kv_sigma, seed, 2).astype(np.uint32) << 16
+    q, k, v = (t.view(np.float32).astype(np.float64) for t in (q, k, v))
+    t0 = time.perf_counter()
+    s = w.scale * (q @ k.T)
+    if w.causal:
+        off = w.Skv - w.Sq if w.causal == 1 else 0
+        s[np.arange(w.Skv)[None, :] > np.arange(w.Sq)[:, None] + off] = -np.inf
+    m = s.max(axis=1, keepdims=True)
+    m[~np.isfinite(m)] = 0.0
+    p = np.exp(s - m)
+    l = p.sum(axis=1, keepdims=True)
+    o = (p @ v) / np.where(l > 0, l, 1.0)
+    dt = time.perf_counter() - t0
+    del o
+    flops = 4 * w.D * visible_pairs(w)
+    return flops / dt / 1e12, dt
+
+
 # ------------------------------------------------------------------ multi-rank helpers
 def max_over_ranks(values, device):
     """Element-wise max of `values` over all ranks of the default process group."""
@@ -352,28 +406,41 @@ def run_ours(args, w):
         if st != fa.ATTN_OK:
             raise fa.AttnError(st, "attn_fwd")
 
-    # ---- warm-up
-    for _ in range(args.warmup):
+    # ---- warm-up (timed too, only to size the timed region)
+    w_start = torch.cuda.Event(enable_timing=True)
+    w_end = torch.cuda.Event(enable_timing=True)
+    for i in range(args.warmup):
         flush.zero_()
+        if i == args.warmup - 1:
+            w_start.record(stream)
         step()
+        if i == args.warmup - 1:
+            w_end.record(stream)
     if fa.attn_check_device_status(stream) != fa.ATTN_OK:
         raise RuntimeError("device status not OK after warm-up")
-
-    # ---- timed: K steps, L2 flushed between steps, events around each launch
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    est_step_s = max(w_start.elapsed_time(w_end) / 1e3, 1e-6)
+    # the K-step block is repeated until the timed region spans min_timed_seconds
+    repeats = max(1, math.ceil(args.min_timed_seconds / (args.steps * (est_step_s + 50e-6))))
     if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
+        repeats = int(max_over_ranks([repeats], dev)[0])
+
+    # ---- timed: repeats x K steps, L2 flushed between steps, events around each launch
+    n_timed = repeats * args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_timed)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n_timed)]
     launches0 = fa.attn_kernel_launches()
     with ClockSampler(local) as clocks:
         t_wall = time.perf_counter()
-        for i in range(args.steps):
-            flush.zero_()
-            starts[i].record(stream)
-            step()
-            ends[i].record(stream)
-        torch.cuda.synchronize(dev)
+        for r in range(repeats):
+            if world > 1:
+                dist.barrier()
+            torch.cuda.synchronize(dev)
+            for i in range(r * args.steps, (r + 1) * args.steps):
+                flush.zero_()
+                starts[i].record(stream)
+                step()
+                ends[i].record(stream)
+            torch.cuda.synchronize(dev)
         t_wall = time.perf_counter() - t_wall
     launches = fa.attn_kernel_launches() - launches0
     if world > 1:
@@ -381,7 +448,10 @@ def run_ours(args, w):
     if fa.attn_check_device_status(stream) != fa.ATTN_OK:
         raise RuntimeError("device status not OK after the timed region")
     times_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    kernel_s = sum(times_ms) / 1e3
+    kernel_s = sum(times_ms) / 1e3 / repeats  # per block of K steps
+
+    # ---- the host link the e2e figure runs over (outside every timed region)
+    link = host_link_rates(dev)
 
     # ---- e2e: pinned host buffers; every step's host->device copies of its inputs
     # and the read of its result are inside the timed region, pipelined over two
@@ -443,6 +513,9 @@ def run_ours(args, w):
     exact = int(fl_mult * exact_flops(w))
     mean_launch_s = kernel_s / args.steps
     achieved = exact / mean_launch_s / 1e12
+    clk = clocks.summary()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    clock_peak = (TENSOR_FLOP_PER_CLK_PER_SM * sms * clk["sm_mhz"] * 1e6 / 1e12) if clk.get("sm_mhz") else None
     bytes_in = q.numel() * 2 + k.numel() * 2 + v.numel() * 2
     bytes_out = o.numel() * 2 + lse.numel() * 4
     if bwd:
@@ -468,23 +541,138 @@ def run_ours(args, w):
                      "kernel": ("attn_bwd step: bwd_prep_kernel + fmha_bwd_dkdv_kernel + "
                                 "fmha_bwd_dq_kernel") if bwd else "attn::fmha_fwd_kernel",
                      "algorithmic_unit": ("10*D FLOPs per visible (q-row, key, q-head)" if bwd else
-                                          "4*D FLOPs per visible (q-row, key, q-head)")},
+                                          "4*D FLOPs per visible (q-row, key, q-head)"),
+                     "clock_matched": {
+                         "peak": clock_peak, "frac": (achieved / clock_peak) if clock_peak else None,
+                         "unit": "TFLOP/s", "flop_per_clk_per_sm": TENSOR_FLOP_PER_CLK_PER_SM,
+                         "sms": sms, "sm_mhz_median": clk.get("sm_mhz"),
+                         "note": "tensor pipe at the SM clock sampled during the timed region "
+                                 "(one 128x128x16 bf16 MMA per 64 cycles per SM, measured)"}},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": bytes_in,
                 "d2h_bytes_per_step": bytes_out, "steps": e2e_steps,
                 "pipelining": "two device buffer sets; uploads and downloads on their own streams "
-                              "overlap the neighbouring steps' kernels"},
+                              "overlap the neighbouring steps' kernels",
+                "host_link_gbs": link,
+                "link_bound": link_bound(link, bytes_in, bytes_out, flops)},
         "gpu_launches": int(launches),
-        "clocks": clocks.summary(),
+        "clocks": clk,
+        "timed_repeats": repeats,
+        "timed_steps_total": n_timed,
         "wall_s_timed_region": t_wall,
         "kernel_ms": {"min": min(times_ms), "median": statistics.median(times_ms),
                       "max": max(times_ms)},
     }
+    if not bwd and args.dtype == "bf16" and args.path == "fwd" and not args.no_other_workloads:
+        line["workloads"] = other_workload_timings(fa, inputs, torch, dev, stream, flush, w.name,
+                                                   rank)
     if world == 1 and not args.no_cpu_baseline and not bwd:
         tf, dt, n, cores = oracle_sample_rate(w, args.cpu_seconds)
         line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": cores, "kind": "oracle",
                                 "sample": f"{n} random query rows of {w.name} "
                                           f"({dt:.1f} s of fp64 oracle work)"}
+        line["cpu_baseline"]["other_points"] = cpu_reference_points(w, args.cpu_seconds)
     print(json.dumps(line), flush=True)
+
+
+def host_link_rates(dev):
+    """Pinned host<->device copy rates (GB/s) of this box: one direction at a
+    time and both at once, 64 MiB per copy, best of three."""
+    import torch
+    n = 64 << 20
+    h_in = torch.empty(n, dtype=torch.uint8).pin_memory()
+    h_out = torch.empty(n, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(n, dtype=torch.uint8, device=dev)
+    d_out = torch.empty(n, dtype=torch.uint8, device=dev)
+    s_up, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    res = {}
+    for name in ("h2d", "d2h", "both"):
+        best = 0.0
+        for _ in range(3):
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            if name in ("h2d", "both"):
+                with torch.cuda.stream(s_up):
+                    d_in.copy_(h_in, non_blocking=True)
+            if name in ("d2h", "both"):
+                with torch.cuda.stream(s_down):
+                    h_out.copy_(d_out, non_blocking=True)
+            torch.cuda.synchronize(dev)
+            dt = time.perf_counter() - t0
+            best = max(best, (2 if name == "both" else 1) * n / dt / 1e9)
+        res[name] = best
+    return res
+
+
+def link_bound(link, bytes_in, bytes_out, flops):
+    """Throughput bound of the e2e step by the host link alone: every step's
+    uploads and downloads at the measured rates (directions overlapped)."""
+    t = max(bytes_in / (link["h2d"] * 1e9), bytes_out / (link["d2h"] * 1e9),
+            (bytes_in + bytes_out) / (link["both"] * 1e9))
+    return {"min_ms_per_step": 1e3 * t, "max_tflops": flops / t / 1e12}
+
+
+def other_workload_timings(fa, inputs, torch, dev, stream, flush, headline: str, rank: int,
+                           warmup: int = 3, steps: int = 10):
+    """Kernel-only attn_fwd throughput of the other benchmark shapes (same
+    timing rules as the headline: events on the launching stream, L2 flushed
+    between steps, inputs resident in HBM)."""
+    import numpy as np
+    out = {}
+    for name in OTHER_WORKLOADS:
+        if name == headline:
+            continue
+        w = inputs.WORKLOADS[name]
+        q_h, k_h, v_h = inputs.make_workload(w, seed=rank)
+
+        def dev_t(bits):
+            return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+
+        q, k, v = dev_t(q_h), dev_t(k_h), dev_t(v_h)
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
+        sh = stream.cuda_stream
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for i in range(warmup + steps):
+            flush.zero_()
+            if i >= warmup:
+                ev[i - warmup][0].record(stream)
+            st = fa.attn_fwd_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                 lse.data_ptr(), w.B, w.Sq, w.Skv, w.Hq, w.Hkv, w.D, w.causal,
+                                 w.scale, sh)
+            if st != fa.ATTN_OK:
+                raise fa.AttnError(st, "attn_fwd")
+            if i >= warmup:
+                ev[i - warmup][1].record(stream)
+        torch.cuda.synchronize(dev)
+        if fa.attn_check_device_status(stream) != fa.ATTN_OK:
+            raise RuntimeError(f"device status not OK after {name}")
+        ms = [a.elapsed_time(b) for a, b in ev]
+        mean_s = sum(ms) / len(ms) / 1e3
+        out[name] = {"value": metric_flops(w) / mean_s / 1e12,
+                     "exact_tflops": exact_flops(w) / mean_s / 1e12,
+                     "ms_per_step": 1e3 * mean_s, "steps": steps, "warmup": warmup,
+                     "entry_point": "attn_fwd"}
+        del q, k, v, o, lse
+    return out
+
+
+def cpu_reference_points(w, target_s: float):
+    """Second CPU reference points: the oracle on one core for the tiny and the
+    headline shapes (larger shapes' one-core figures would be extrapolations),
+    and numpy fp64 (BLAS) on one (batch, head) slice of the workload."""
+    from attention_forward_11_gb300 import inputs
+    pts = {}
+    for name in ("tiny_causal", "mha_causal_4x16x4096"):
+        tf, dt, n, cores = oracle_one_core(name, min(target_s, 6.0))
+        pts[f"oracle_1core_{name}"] = {"value": tf, "unit": UNIT, "cores": cores,
+                                       "sample": f"{n} random query rows ({dt:.1f} s)"}
+    tf, dt = numpy_fp64_rate(w)
+    pts["numpy_fp64_blas"] = {"value": tf, "unit": UNIT, "cores": os.cpu_count(),
+                              "sample": f"one (batch, head) slice of {w.name}: {w.Sq} x {w.Skv} "
+                                        f"dense masked logits ({dt:.2f} s)"}
+    del inputs
+    return pts
 
 
 def main():
@@ -498,6 +686,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="skip the kernel-only timings of the other benchmark shapes")
+    ap.add_argument("--min-timed-seconds", type=float, default=1.0,
+                    help="repeat the K-step block until the timed region spans this long")
     ap.add_argument("--dtype", choices=["bf16", "f16"], default="bf16",
                     help="element type of Q, K, V, O (f16 goes through attn_fwd_ex)")
     ap.add_argument("--path", choices=["fwd", "splitkv", "bwd"], default="fwd",

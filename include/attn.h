@@ -17,8 +17,12 @@
  * tutorial's non-persistent FA kernel, on Blackwell tensor cores (tcgen05).
  *
  * Plain pointers and sizes only; no framework types.  All functions are
- * thread-safe.  The library allocates no device memory: scratch memory, where a
- * path needs some, is passed in by the caller.
+ * thread-safe.  No call allocates device memory: scratch memory, where a path
+ * needs some, is passed in by the caller.  The library's own device state is
+ * static: a 4-byte status word and the 40 MiB scratch array of
+ * attn_fwd_splitkv_noalloc, which every GPU that loads the library holds until
+ * the process exits (one copy per GPU), whether or not that entry point is
+ * ever called.
  */
 #ifndef LIBATTN_ATTN_H_
 #define LIBATTN_ATTN_H_
@@ -35,7 +39,7 @@ typedef enum {
     ATTN_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment, scale or flag; nothing launched */
     ATTN_ERR_UNSUPPORTED = 2, /* valid request this build does not implement (head size)  */
     ATTN_ERR_CUDA = 3,        /* a CUDA runtime/driver call or the kernel launch failed       */
-    ATTN_ERR_TIMEOUT = 4      /* a device-side bounded wait ran out (see attn_check_device_status) */
+    ATTN_ERR_TIMEOUT = 4      /* a device-side bounded wait ran out (see attn_last_device_status) */
 } attn_status_t;
 
 /*
@@ -59,7 +63,7 @@ typedef enum {
  * Ownership: the caller owns every buffer; nothing is retained after return.
  * q, k, v, o must be 16-byte aligned (TMA).  o must not alias q, k or v.
  * Returns ATTN_OK once the kernel is enqueued; a device-side wait that runs out
- * is reported later through attn_check_device_status.  On any error return,
+ * is reported later through attn_last_device_status.  On any error return,
  * nothing was launched and no output was written.
  */
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
@@ -126,10 +130,12 @@ attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void
  *     capture begins.
  *   - Problems whose scratch would exceed 40 MiB return ATTN_ERR_UNSUPPORTED
  *     (on a 152-SM GPU the split plan never needs more than about 38.4 MiB).
- *   - Every call shares the one array, which keeps the last call's contents;
- *     nothing in it needs to start at zero (each call writes every partial slot
- *     before it reads it).  Calls that overlap in time on the GPU (different
- *     streams, or devices sharing the process's array) race on it: serialise them.
+ *   - Each GPU has its own copy of the array; every call on one GPU shares that
+ *     copy, which keeps the last call's contents.  Nothing in it needs to start
+ *     at zero (each call writes every partial slot before it reads it).  Calls
+ *     that overlap in time on the same GPU (for example on different streams)
+ *     race on it and must be serialised; calls on different GPUs do not share
+ *     scratch.
  */
 attn_status_t attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
                                        float* lse, int B, int Sq, int Skv, int Hq, int Hkv, int D,
@@ -167,7 +173,7 @@ attn_status_t attn_fwd_splitkv_noalloc(const void* q, const void* k, const void*
  * 16-byte aligned; lse 4-byte aligned.  dq, dk, dv and the workspace must not
  * overlap any input or each other.  Three kernels are enqueued on `stream`
  * (prep, dK/dV, dQ); errors are reported as for attn_fwd (nothing is launched
- * on any error return; a device-side timeout shows in attn_check_device_status).
+ * on any error return; a device-side timeout shows in attn_last_device_status).
  */
 attn_status_t attn_bwd_workspace_size(int B, int Sq, int Skv, int Hq, int Hkv, int D, size_t* bytes);
 attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -179,10 +185,24 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
 const char* attn_status_str(attn_status_t status);
 
 /*
- * Synchronises `stream`, then reads and clears this device's kernel status
- * word.  Returns ATTN_ERR_TIMEOUT if any libattn kernel on the current device
- * gave up a bounded wait since the last check (its outputs are then invalid),
- * ATTN_ERR_CUDA if synchronisation itself failed, else ATTN_OK.
+ * attn_last_device_status -- the device-side outcome of the calls made so far.
+ * Every libattn kernel records a bounded wait that ran out in one status word
+ * per device (the Pallas page's host boundary returns errors only at call
+ * time; this word carries the ones found later, on the GPU).  Waits until all
+ * work submitted to the current device has completed (cudaDeviceSynchronize),
+ * then reads and clears that device's word.  Returns ATTN_ERR_TIMEOUT if any
+ * libattn kernel on the current device gave up a bounded wait since the word
+ * was last read (that call's outputs are then invalid), ATTN_ERR_CUDA if
+ * synchronisation or the read failed, else ATTN_OK.  The word is per device,
+ * not per calling thread: a timeout is reported once, to whichever caller
+ * reads it first.
+ */
+attn_status_t attn_last_device_status(void);
+
+/*
+ * attn_check_device_status -- attn_last_device_status that waits only for
+ * `stream` (cudaStreamSynchronize) instead of the whole device, for callers
+ * whose libattn work all ran on that stream.  Same word, same return values.
  */
 attn_status_t attn_check_device_status(cudaStream_t stream);
 
@@ -194,7 +214,7 @@ unsigned long long attn_kernel_launches(void);
  * launches one CTA that waits on an mbarrier nothing ever arrives on, for at
  * most `poll_limit` polls, then records ATTN_ERR_TIMEOUT in the device status
  * word and returns normally.  The caller then sees ATTN_ERR_TIMEOUT from
- * attn_check_device_status.  poll_limit must be in [1, 1<<20].
+ * attn_last_device_status.  poll_limit must be in [1, 1<<20].
  */
 attn_status_t attn_debug_wait_timeout(unsigned int poll_limit, cudaStream_t stream);
 
@@ -215,10 +235,11 @@ attn_status_t attn_debug_wait_timeout(unsigned int poll_limit, cudaStream_t stre
  *   out[6]     exponentials per cycle per SM (= 4 x 32 / out[5])
  *   out[7]     number of SMs measured
  * Returns ATTN_ERR_INVALID_ARG for a NULL `out` or n < ATTN_UNIT_RATES (nothing
- * is launched), ATTN_ERR_CUDA on a launch or copy failure, and otherwise the
- * result of attn_check_device_status(stream): ATTN_ERR_TIMEOUT if the MMA
- * completion wait ran out, or if any earlier libattn kernel's bounded wait had
- * (the device status word is read and cleared, as that call does).
+ * is launched), ATTN_ERR_CUDA on a launch or copy failure, ATTN_ERR_TIMEOUT if
+ * the MMA completion wait ran out or if an earlier libattn kernel on this device
+ * had already recorded a timeout (that earlier timeout is reported here, not
+ * lost: the status word is read and cleared before the first rate kernel and
+ * again after the last, as attn_check_device_status(stream) does), else ATTN_OK.
  */
 #define ATTN_UNIT_RATES 8
 attn_status_t attn_debug_unit_rates(double* out, int n, cudaStream_t stream);

@@ -140,3 +140,18 @@ def test_reference_arm_prints_one_contract_line():
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_link_bound_takes_the_slowest_direction(bench):
+    link = {"h2d": 200.0, "d2h": 100.0, "both": 250.0}
+    b = bench.link_bound(link, 200e9 * 1e-3, 50e9 * 1e-3, 1e12)   # 1 ms up, 0.5 ms down, 1 ms both
+    assert abs(b["min_ms_per_step"] - 1.0) < 1e-9
+    assert abs(b["max_tflops"] - 1000.0) < 1e-6
+    link = {"h2d": 200.0, "d2h": 200.0, "both": 250.0}
+    b = bench.link_bound(link, 100e6, 100e6, 1e12)                  # both directions at once bind
+    assert abs(b["min_ms_per_step"] - 0.8) < 1e-9
+
+
+def test_numpy_point_counts_the_visible_pairs(bench):
+    tf, dt = bench.numpy_fp64_rate(inputs.WORKLOADS["tiny_causal"])
+    assert tf > 0 and dt > 0

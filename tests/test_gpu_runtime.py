@@ -23,6 +23,27 @@ def test_timeout_is_reported_and_cleared():
     check_full(q, k, v, 1, 1 / math.sqrt(128), "after timeout self-test")
 
 
+def test_last_device_status_reports_a_timeout_once():
+    """The boundary's stream-less status call: it waits for the whole device,
+    so it sees the self-test kernel's timeout without being given its stream."""
+    import torch
+    assert fa.attn_last_device_status() == fa.ATTN_OK
+    side = torch.cuda.Stream()
+    assert fa.attn_debug_wait_timeout(1000, side) == fa.ATTN_OK
+    assert fa.attn_last_device_status() == fa.ATTN_ERR_TIMEOUT
+    assert fa.attn_last_device_status() == fa.ATTN_OK
+    assert fa.attn_check_device_status() == fa.ATTN_OK
+
+
+def test_unit_rates_keep_an_earlier_timeout():
+    """A timeout recorded before the diagnostic runs is reported by it, not wiped."""
+    assert fa.attn_debug_wait_timeout(1000) == fa.ATTN_OK
+    with pytest.raises(fa.AttnError) as e:
+        fa.attn_debug_unit_rates()
+    assert e.value.status == fa.ATTN_ERR_TIMEOUT
+    assert fa.attn_last_device_status() == fa.ATTN_OK
+
+
 def test_one_launch_per_call():
     import torch
     q, k, v = inputs.make_qkv(1, 256, 256, 2, 2, 128, seed=1)

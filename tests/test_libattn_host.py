@@ -31,6 +31,30 @@ def test_header_declares_expected_entry_points():
     assert declared_functions() == sorted(fa._binding.EXPORTED)
 
 
+def _declaration(name):
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    m = re.search(r"(\w+)\s+" + name + r"\s*\(([^)]*)\)\s*;", text)
+    assert m, f"{name} is not declared"
+    params = [" ".join(p.split()) for p in m.group(2).split(",")]
+    return m.group(1), params
+
+
+def test_boundary_calls_have_the_surveyed_signatures():
+    """The three calls of the boundary: the forward, the status string, and the
+    device status of the calls made so far (no stream argument)."""
+    ret, params = _declaration("attn_fwd")
+    assert ret == "attn_status_t"
+    assert params == ["const void* q", "const void* k", "const void* v", "void* o", "float* lse",
+                      "int B", "int Sq", "int Skv", "int Hq", "int Hkv", "int D", "int causal",
+                      "float scale", "cudaStream_t stream"]
+    assert re.search(r"const char\*\s*attn_status_str\(attn_status_t status\);", open(HEADER).read())
+    assert _declaration("attn_last_device_status") == ("attn_status_t", ["void"])
+    text = open(HEADER).read()
+    for name, value in (("ATTN_OK", 0), ("ATTN_ERR_INVALID_ARG", 1), ("ATTN_ERR_UNSUPPORTED", 2),
+                        ("ATTN_ERR_CUDA", 3), ("ATTN_ERR_TIMEOUT", 4)):
+        assert re.search(rf"\b{name}\s*=\s*{value}\b", text), name
+
+
 def test_every_declared_symbol_is_exported(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name
@@ -63,7 +87,8 @@ def call(**over):
     dict(Hq=6, Hkv=4), dict(causal=3), dict(causal=-1),
     dict(scale=0.0), dict(scale=-1.0), dict(scale=math.nan), dict(scale=math.inf),
     dict(q=Q + 8), dict(k=K + 2), dict(v=V + 4), dict(o=O + 1), dict(lse=L + 2),
-    dict(o=Q + 64), dict(o=K), dict(lse=O + 16),
+    dict(o=Q + 64), dict(o=K), dict(lse=O + 16), dict(lse=Q + 32), dict(lse=K + 64),
+    dict(lse=V), dict(lse=V + 256 * 2 * 128 * 2 - 4),
 ], ids=lambda d: ",".join(f"{k}={v}" for k, v in d.items()))
 def test_invalid_arguments_rejected(lib, over):
     assert call(**over) == fa.ATTN_ERR_INVALID_ARG

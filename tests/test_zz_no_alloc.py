@@ -7,9 +7,12 @@ a workspace the caller passes.  This file is collected last on purpose, so a
 run that stops at its first failure has already run every other test; it also
 passes on its own in a fresh process.
 
-The check: through the C ABI, two calls in a row of the no-allocation entry
-point against the existing split-KV entry point (with a caller workspace), on
-shapes that do split, within the parity tolerance the other GPU tests use.
+The checks, through the C ABI, two calls in a row each: the no-allocation entry
+point runs the same plan and the same kernels as attn_fwd_splitkv with a caller
+workspace, so its O and LSE must be bit-identical to that entry point's, and it
+must launch the same kernels (two when the plan splits: the split forward and
+the combine; one when it does not).  One shape is also compared with the fp64
+oracle directly, and one takes the no-split fallback.
 """
 import math
 
@@ -37,37 +40,78 @@ def _device(bits):
 
 
 CASES = [
-    # B, Sq, Skv, Hq, Hkv, causal: few query tiles against long key ranges (split)
-    (1, 256, 8192, 2, 2, 1),
-    (1, 300, 5000, 4, 2, 2),
-    (1, 512, 32768, 64, 8, 1),
+    # B, Sq, Skv, Hq, Hkv, D, causal: few query tiles against long key ranges (split) ...
+    (1, 256, 8192, 2, 2, 128, 1),
+    (1, 300, 5000, 4, 2, 128, 2),
+    (1, 256, 6000, 4, 4, 64, 0),
+    (1, 512, 32768, 64, 8, 128, 1),
+    # ... and one with more units than the split plan takes: the plain schedule, no scratch
+    (9, 2048, 2048, 16, 16, 64, 1),
 ]
+
+
+def _noalloc(q, k, v, B, Sq, Skv, Hq, Hkv, D, causal, scale):
+    import torch
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((B, Hq, Sq), float("nan"), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    before = fa.attn_kernel_launches()
+    st = fa.attn_fwd_splitkv_noalloc_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                         lse.data_ptr(), B, Sq, Skv, Hq, Hkv, D, causal, scale,
+                                         stream)
+    assert st == fa.ATTN_OK, fa.attn_status_str(st)
+    launched = fa.attn_kernel_launches() - before
+    assert fa.attn_check_device_status() == fa.ATTN_OK
+    return o, lse, launched
 
 
 @pytest.mark.parametrize("case", CASES, ids=[str(c) for c in CASES])
 def test_noalloc_matches_workspace_entry_point_twice(case):
     import torch
-    B, Sq, Skv, Hq, Hkv, causal = case
-    D, scale = 128, 1 / math.sqrt(128)
+    B, Sq, Skv, Hq, Hkv, D, causal = case
+    scale = 1 / math.sqrt(D)
     q, k, v = (_device(t) for t in inputs.make_qkv(B, Sq, Skv, Hq, Hkv, D, seed=sum(case)))
-    assert fa.attn_fwd_splitkv_workspace_size(B, Sq, Skv, Hq, Hkv, D, causal) > 0
+    ws = fa.attn_fwd_splitkv_workspace_size(B, Sq, Skv, Hq, Hkv, D, causal)
+    before = fa.attn_kernel_launches()
     o_ref, l_ref = fa.attn_fwd_splitkv(q, k, v, causal=causal, scale=scale)
+    expected_launches = fa.attn_kernel_launches() - before
+    assert expected_launches == (2 if ws > 0 else 1)
     assert fa.attn_check_device_status() == fa.ATTN_OK
-    stream = torch.cuda.current_stream().cuda_stream
     for call in range(2):  # the static scratch keeps the previous call's contents
-        o = torch.full_like(q, float("nan"))
-        lse = torch.full((B, Hq, Sq), float("nan"), dtype=torch.float32, device="cuda")
-        st = fa.attn_fwd_splitkv_noalloc_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(),
-                                             o.data_ptr(), lse.data_ptr(), B, Sq, Skv, Hq, Hkv,
-                                             D, causal, scale, stream)
-        assert st == fa.ATTN_OK, fa.attn_status_str(st)
-        assert fa.attn_check_device_status() == fa.ATTN_OK
-        assert torch.isfinite(o.float()).all(), f"call {call}: non-finite O"
-        err = (o.float() - o_ref.float()).abs()
-        assert err.max().item() <= O_MAX_ABS and err.mean().item() <= O_MEAN_ABS, f"call {call}"
-        ninf = torch.isneginf(l_ref)
-        assert torch.equal(torch.isneginf(lse), ninf), f"call {call}: -inf LSE pattern"
-        assert (lse[~ninf] - l_ref[~ninf]).abs().max().item() <= LSE_MAX_ABS, f"call {call}"
+        o, lse, launched = _noalloc(q, k, v, B, Sq, Skv, Hq, Hkv, D, causal, scale)
+        assert launched == expected_launches, f"call {call}: {launched} kernels launched"
+        assert torch.equal(o, o_ref), f"call {call}: O differs from attn_fwd_splitkv"
+        assert torch.equal(lse, l_ref), f"call {call}: LSE differs from attn_fwd_splitkv"
+
+
+def test_noalloc_takes_the_plain_schedule_when_nothing_splits():
+    import torch
+    B, Sq, Skv, Hq, Hkv, D, causal = CASES[-1]
+    assert fa.attn_fwd_splitkv_workspace_size(B, Sq, Skv, Hq, Hkv, D, causal) == 0
+    q, k, v = (_device(t) for t in inputs.make_qkv(B, Sq, Skv, Hq, Hkv, D, seed=5))
+    o_ref, l_ref = fa.attn_fwd(q, k, v, causal=causal, scale=1 / math.sqrt(D))
+    o, lse, launched = _noalloc(q, k, v, B, Sq, Skv, Hq, Hkv, D, causal, 1 / math.sqrt(D))
+    assert launched == 1
+    assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
+
+
+def test_noalloc_against_the_oracle():
+    import oracle
+    B, Sq, Skv, Hq, Hkv, D, causal = 1, 300, 5000, 4, 2, 128, 1
+    scale = 1 / math.sqrt(D)
+    qb, kb, vb = inputs.make_qkv(B, Sq, Skv, Hq, Hkv, D, seed=11, q_sigma=4.0)
+    assert fa.attn_fwd_splitkv_workspace_size(B, Sq, Skv, Hq, Hkv, D, causal) > 0
+    q, k, v = _device(qb), _device(kb), _device(vb)
+    o_ref, l_ref = oracle.attn_full(qb, kb, vb, causal, scale)
+    o_ref = oracle.round_bf16(o_ref)
+    for call in range(2):
+        o, lse, _ = _noalloc(q, k, v, B, Sq, Skv, Hq, Hkv, D, causal, scale)
+        err = np.abs(o.float().double().cpu().numpy() - o_ref)
+        assert err.max() <= O_MAX_ABS and err.mean() <= O_MEAN_ABS, f"call {call}"
+        l64 = lse.double().cpu().numpy()
+        ninf = np.isneginf(l_ref)
+        assert np.array_equal(np.isneginf(l64), ninf), f"call {call}: -inf LSE pattern"
+        assert np.abs(l64[~ninf] - l_ref[~ninf]).max() <= LSE_MAX_ABS, f"call {call}"
 
 
 def test_noalloc_rejects_bad_arguments_without_launch():
