@@ -186,6 +186,20 @@ struct SplitPlan {
     attn::CombineTable comb{};
 };
 constexpr size_t kWorkspaceAlign = 256;
+// Split only when the whole-unit makespan is at least ATTN_SPLIT_MARGIN_PCT percent
+// of the split share plus ATTN_SPLIT_MIN_STEPS KV iterations.  Measured on GB300
+// over few-tile shapes (Sq 1-2048, Skv 8K-128K, GQA 8/1, 32/8, 64/8, MHA 16): every
+// shape with a ratio of 2.4 or more gained 1.5-19x from the split; between 1.15
+// and 1.33 the outcome ranged from 0.89x to 1.34x (the benchmark's chunked
+// prefill, 1.19: 0.96x), so those keep the whole-unit schedule.  (Building with
+// both set to 0 splits wherever the plan can: how the crossover was measured.)
+#ifndef ATTN_SPLIT_MARGIN_PCT
+#define ATTN_SPLIT_MARGIN_PCT 135
+#endif
+#ifndef ATTN_SPLIT_MIN_STEPS
+#define ATTN_SPLIT_MIN_STEPS 4
+#endif
+constexpr long long kSplitMarginPct = ATTN_SPLIT_MARGIN_PCT, kSplitMinSteps = ATTN_SPLIT_MIN_STEPS;
 
 size_t workspace_bytes_for(int n_slots, int D) {
     const size_t o_bytes = (size_t)n_slots * attn::kTiles * attn::kBM * D * sizeof(float);
@@ -215,6 +229,25 @@ void build_split_plan(const attn::FwdParams& p, int sms, SplitPlan* plan) {
     }
     const int G = static_cast<int>(std::min<long long>(std::min(sms, attn::kMaxSplitCtas), T));
     if (G < 1) return;
+    // Does a split pay?  The whole-unit schedule takes as long as its busiest CTA
+    // (units in the snake order over min(#units, #SMs) CTAs); the split one about
+    // ceil(T / G) iterations, but its shares start at different KV positions, so the
+    // L2 sharing of each K/V tile between the units of a head that run side by side
+    // is lost, and a merge kernel follows.  Split only when the whole-unit makespan
+    // exceeds the share by the measured margin.
+    {
+        const int Gp = std::min(p.n_units, std::min(sms, attn::kMaxPieces));
+        long long load[attn::kMaxPieces] = {};
+        long long makespan = 0;
+        for (int u = 0; u < p.n_units; ++u) {
+            const int r = u / Gp, c = u % Gp;
+            const int cta = (r & 1) ? Gp - 1 - c : c;
+            load[cta] += W[u];
+            makespan = std::max(makespan, load[cta]);
+        }
+        const long long share = (T + G - 1) / G;
+        if (makespan * 100 < share * kSplitMarginPct + kSplitMinSteps * 100) return;
+    }
     for (int c = 0; c <= G; ++c) bnd[c] = (long long)c * T / G;
     attn::SplitSched& sc = plan->sched;
     attn::CombineTable& cb = plan->comb;

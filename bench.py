@@ -675,6 +675,81 @@ def cpu_reference_points(w, target_s: float):
     return pts
 
 
+SWEEP_SHAPES = [(1, hq, hkv, sq, skv) for (hq, hkv) in ((8, 1), (64, 8), (32, 8), (16, 16))
+                for sq in (1, 128, 512, 1024, 2048) for skv in (8192, 32768, 131072)] + [
+    (4, 32, 8, 128, 32768), (4, 64, 8, 512, 32768), (2, 16, 16, 1024, 65536), (8, 8, 1, 1, 32768),
+    (2, 8, 8, 256, 16384)]
+
+
+def splitkv_sweep(args):
+    """attn_fwd against attn_fwd_splitkv (the planner's own choice, with the
+    workspace it asks for) on few-tile shapes: bottom-right causal, D = 128,
+    seeded normal inputs made on the device (timing only; parity is the tests'
+    job).  One JSON line per shape: median of `--steps` launches each, L2 flushed
+    between launches."""
+    import torch
+    import attention_forward_11_gb300 as fa
+    from attention_forward_11_gb300 import build as libbuild
+    libbuild.build()
+    fa.load_library()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    gen = torch.Generator(device=dev)
+    D = 128
+
+    def median_ms(fn):
+        for _ in range(args.warmup):
+            flush.zero_()
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+    for (B, Hq, Hkv, Sq, Skv) in SWEEP_SHAPES:
+        gen.manual_seed(B * 7 + Hq + Sq + Skv)
+        q = torch.randn(B, Sq, Hq, D, device=dev, generator=gen).to(torch.bfloat16)
+        k = torch.randn(B, Skv, Hkv, D, device=dev, generator=gen).to(torch.bfloat16)
+        v = torch.randn(B, Skv, Hkv, D, device=dev, generator=gen).to(torch.bfloat16)
+        o = torch.empty_like(q)
+        lse = torch.empty(B, Hq, Sq, dtype=torch.float32, device=dev)
+        ws_n = fa.attn_fwd_splitkv_workspace_size(B, Sq, Skv, Hq, Hkv, D, 1)
+        ws = torch.empty(max(ws_n, 1), dtype=torch.uint8, device=dev)
+        sc = 1.0 / math.sqrt(D)
+
+        def plain():
+            st = fa.attn_fwd_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                 B, Sq, Skv, Hq, Hkv, D, 1, sc, sh)
+            if st != fa.ATTN_OK:
+                raise fa.AttnError(st, "attn_fwd")
+
+        def split():
+            st = fa.attn_fwd_splitkv_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                         lse.data_ptr(), B, Sq, Skv, Hq, Hkv, D, 1, sc, ws.data_ptr(),
+                                         ws_n, sh)
+            if st != fa.ATTN_OK:
+                raise fa.AttnError(st, "attn_fwd_splitkv")
+
+        tp, ts = median_ms(plain), median_ms(split)
+        if fa.attn_check_device_status(stream) != fa.ATTN_OK:
+            raise RuntimeError("device status not OK in the split-KV sweep")
+        w = type("W", (), dict(B=B, Hq=Hq, Sq=Sq, Skv=Skv, D=D, causal=1))
+        fl = exact_flops(w)
+        print(json.dumps({"B": B, "Hq": Hq, "Hkv": Hkv, "Sq": Sq, "Skv": Skv, "D": D, "causal": 1,
+                          "split": ws_n > 0, "workspace_bytes": ws_n, "attn_fwd_ms": tp,
+                          "attn_fwd_splitkv_ms": ts, "attn_fwd_tflops": fl / tp / 1e9,
+                          "attn_fwd_splitkv_tflops": fl / ts / 1e9, "gain": tp / ts}), flush=True)
+        del q, k, v, o, lse, ws
+
+
 def main():
     from attention_forward_11_gb300 import inputs
     ap = argparse.ArgumentParser()
@@ -690,6 +765,9 @@ def main():
                     help="skip the kernel-only timings of the other benchmark shapes")
     ap.add_argument("--min-timed-seconds", type=float, default=1.0,
                     help="repeat the K-step block until the timed region spans this long")
+    ap.add_argument("--splitkv-sweep", action="store_true",
+                    help="time attn_fwd against attn_fwd_splitkv on few-tile shapes (one JSON "
+                         "line per shape) instead of the benchmark")
     ap.add_argument("--dtype", choices=["bf16", "f16"], default="bf16",
                     help="element type of Q, K, V, O (f16 goes through attn_fwd_ex)")
     ap.add_argument("--path", choices=["fwd", "splitkv", "bwd"], default="fwd",
@@ -700,6 +778,10 @@ def main():
     if args.dtype == "f16" and args.path == "splitkv":
         ap.error("the split-KV entry points take bf16")
     w = inputs.WORKLOADS[args.workload]
+    if args.splitkv_sweep:
+        args.steps = min(args.steps, 10)
+        splitkv_sweep(args)
+        return
     if args.impl == "reference":
         run_reference(args, w)
     else:

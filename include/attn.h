@@ -101,6 +101,11 @@ attn_status_t attn_fwd_ex(const void* q, const void* k, const void* v, void* o, 
  * attn_fwd_splitkv_workspace_size: bytes of workspace attn_fwd_splitkv needs
  *   for this problem on the current device (it depends on the SM count); 0 when
  *   no split pays off, and then attn_fwd_splitkv runs exactly what attn_fwd runs.
+ *   A split is chosen only when the whole-unit schedule's busiest SM would run at
+ *   least 1.35x the KV iterations of an equal share (plus 4): the crossover
+ *   measured on GB300 (decode rows and short prefill chunks against long key
+ *   ranges split and run several times faster; shapes that already fill the GPU
+ *   do not).  This is the entry point to call when scratch can be supplied.
  * attn_fwd_splitkv: workspace device pointer (256-byte aligned, not aliasing
  *   any other argument) of at least that many bytes, or NULL when the size is 0.
  *   The workspace is scratch: its contents are undefined before and after the

@@ -46,7 +46,8 @@ def test_d64_full_size_sampled_rows():
     check_rows(q, k, v, 1, 1 / math.sqrt(D), rows, "mha causal d64")
 
 
-@pytest.mark.parametrize("case", [(1, 256, 8192, 2, 2, 1), (1, 300, 5000, 4, 2, 2)],
+# shapes the planner splits (few query tiles against many KV tiles)
+@pytest.mark.parametrize("case", [(1, 256, 8192, 2, 2, 1), (1, 2048, 4096, 2, 2, 2)],
                          ids=["br", "tl"])
 def test_d64_splitkv_every_row(case):
     B, Sq, Skv, Hq, Hkv, causal = case
