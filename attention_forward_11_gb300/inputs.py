@@ -51,6 +51,8 @@ WORKLOADS = {
     # the headline shape at head sizes 64 and 256 (the Pallas page's benchmark sweeps 64, 128, 256)
     "mha_causal_4x16x4096_d64": Workload("mha_causal_4x16x4096_d64", 4, 16, 16, 4096, 4096, 64, 1),
     "mha_causal_4x16x4096_d256": Workload("mha_causal_4x16x4096_d256", 4, 16, 16, 4096, 4096, 256, 1),
+    # a decode-like split-KV shape: one query row per sequence against 32K keys, GQA 8/1
+    "decode_gqa_8x1_b8_1x32768": Workload("decode_gqa_8x1_b8_1x32768", 8, 8, 1, 1, 32768, 128, 1),
 }
 
 HEADLINE = "mha_causal_4x16x4096"
