@@ -23,7 +23,10 @@
 //                MMA warp waits once per KV step, for both operands of that step
 //                (P.V with V_j, then S_{j+1} with K_{j+1}), and releases both with
 //                one commit
-//   warps 14-15  idle
+//   warp  14     release warp: once any bounded wait of the CTA has run out, it
+//                completes the MMA warp's P barriers (below) until that warp has
+//                left its loop
+//   warp  15     idle
 // Registers are split with setmaxnreg: softmax 176, epilogue 88, MMA/producer 72
 // per thread (2*176 + 88 + 72 = 4 * 128, the launch allocation of 128 per thread).
 //
@@ -41,6 +44,13 @@
 // and O in tensor memory is rescaled only on the rare tiles that raise it.
 // The weights of a tile are handed to the MMA warp in two halves of 64 keys, so
 // the first half of O += P.V runs while the second half's exponentials are made.
+// That hand-off uses hardware named barriers (softmax warps arrive, the MMA warp
+// syncs), not mbarriers: an mbarrier poll by the warp that issued tcgen05.mma
+// returns only after that warp's queued MMAs have drained, which left the tensor
+// core idle between every group of MMAs, while a named barrier does not wait for
+// them.  Each such barrier completes once per (tile, half, KV step): the softmax
+// warps of a tile can arrive for step k+1 only after S_t(k+1) exists, which the
+// MMA warp issues after its sync for step k, so generations never mix.
 //
 // Causal masks (bottom-right aligned: key j visible from row i iff j <= i + Skv - Sq;
 // top-left aligned: iff j <= i): KV tiles entirely above a tile's last visible key
@@ -50,7 +60,10 @@
 // Every mbarrier wait is bounded: when a wait runs out, the thread records
 // ATTN_ERR_TIMEOUT in the device status word and raises a CTA abort flag; all
 // roles then leave their loops, in-flight TMA loads and MMAs are drained with
-// bounded waits, and tensor memory is freed before the CTA exits.
+// bounded waits, and tensor memory is freed before the CTA exits.  A named
+// barrier cannot time out, so once the abort flag is up the release warp keeps
+// arriving on the MMA warp's P barriers (with the softmax warps' thread count)
+// until the MMA warp reports that it has left its loop.
 #pragma once
 #include <cstdint>
 #include <type_traits>
@@ -70,6 +83,11 @@ constexpr int kSoftmaxWarps = 4 * kTiles;          // warpgroups 0 and 1
 constexpr int kEpilogueWarp0 = kSoftmaxWarps;      // warpgroup 2
 constexpr int kMmaWarp = kEpilogueWarp0 + 4;       // warpgroup 3
 constexpr int kLoadWarp = kMmaWarp + 1;
+constexpr int kReleaseWarp = kMmaWarp + 2;
+// named barriers: 1 = epilogue staging; kBarP + 2 t + h = P_t half h in tensor memory
+// (the tile's four softmax warps arrive, the MMA warp syncs)
+constexpr uint32_t kBarP = 2;
+constexpr uint32_t kBarPThreads = 4 * 32 + 32;
 constexpr int kThreads = 512;
 constexpr int kRegsSoftmax = 176, kRegsEpilogue = 88, kRegsOther = 72;
 static_assert(2 * kRegsSoftmax + kRegsEpilogue + kRegsOther <= 4 * (65536 / kThreads),
@@ -85,8 +103,7 @@ enum : int {
     BAR_KVFULL = BAR_QEMPTY + kTiles,        // [stage]: V_{g-1} and K_g landed
     BAR_KVEMPTY = BAR_KVFULL + kStages,      // [stage]: both read by their last MMA
     BAR_SFULL = BAR_KVEMPTY + kStages,
-    BAR_PFULL = BAR_SFULL + kTiles,          // [tile][half]: P of 64 keys in TMEM
-    BAR_ODONE = BAR_PFULL + 2 * kTiles,
+    BAR_ODONE = BAR_SFULL + kTiles,
     BAR_OFREE = BAR_ODONE + kTiles,
     BAR_STATSFULL = BAR_OFREE + kTiles,
     BAR_STATSFREE = BAR_STATSFULL + kTiles,
@@ -109,7 +126,8 @@ struct Geo {
     static constexpr int kSmemBar = kSmemStats + kTiles * kBM * 8;
     static constexpr int kSmemTmemSlot = kSmemBar + BAR_COUNT * 8;
     static constexpr int kSmemAbort = kSmemTmemSlot + 4;
-    static constexpr int kSmemUsed = kSmemAbort + 4;
+    static constexpr int kSmemMmaExit = kSmemAbort + 4;  // set once the MMA warp left its loop
+    static constexpr int kSmemUsed = kSmemMmaExit + 4;
     static constexpr int kSmemBytes = kSmemUsed + 1024;  // + slack to align the base to 1024 bytes
     static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
 };
@@ -297,6 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) / 32, 0);
     const int lane = static_cast<int>(threadIdx.x) & 31;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + G::kSmemAbort);
+    volatile int* mma_exit = reinterpret_cast<volatile int*>(smem + G::kSmemMmaExit);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::kSmemTmemSlot);
     auto bar = [&](int i) -> uint32_t { return sbase + G::kSmemBar + 8 * i; };
 
@@ -306,8 +325,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(BAR_QFULL + t), 1);
             mbar_init(bar(BAR_QEMPTY + t), 1);
             mbar_init(bar(BAR_SFULL + t), 1);
-            mbar_init(bar(BAR_PFULL + 2 * t), 4 * 32);
-            mbar_init(bar(BAR_PFULL + 2 * t + 1), 4 * 32);
             mbar_init(bar(BAR_ODONE + t), 1);
             mbar_init(bar(BAR_OFREE + t), 4 * 32);
             mbar_init(bar(BAR_STATSFULL + t), 4 * 32);
@@ -319,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(bar(BAR_MMADONE), 1);
         *abort_flag = 0;
+        *mma_exit = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
@@ -464,7 +482,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         };
         int kv = 0;                 // KV tiles consumed so far (stage kv carries K_kv)
-        int sc0 = 0, sc1 = 0;       // S_t products issued so far (s_full / p_full phase)
         bool ok = true;
         for (int j = 0; ok; ++j) {
             Unit w;
@@ -490,9 +507,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (w.n(t) <= 1) mma_commit(bar(BAR_QEMPTY + t));  // Q_t no longer read
                 }
                 __syncwarp();
-                if (w.n(t) > 0) {
-                    if (t == 0) ++sc0; else ++sc1;
-                }
             }
             if (!ok) break;
             if (nm > 0) {  // stage kv: its V was read by the previous unit's last P.V, its K now
@@ -510,7 +524,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int t = 0; t < kTiles; ++t) {
                     const int nt = w.n(t);
                     if (kt < nt) {
-                        const int sc = t ? sc1 : sc0;
                         // the first P.V of a unit overwrites O_t: the previous unit's
                         // epilogue must have read it out of tensor memory
                         if (kt == 0 && j > 0 &&
@@ -521,10 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // P_t(kt) arrives in two halves of 64 keys; each half's P.V starts
                         // as soon as the softmax warpgroup has stored it
                         for (int h = 0; h < 2; ++h) {
-                            if (!wait_bounded(bar(BAR_PFULL + 2 * t + h), (sc - 1) & 1, abort_flag, limit)) {
-                                ok = false;
-                                break;
-                            }
+                            named_bar_sync(kBarP + 2 * t + h, kBarPThreads);
                             tc_fence_after();
                             if (elect_one()) {
                                 issue_pv(t, vs, h, kt > 0);
@@ -551,7 +561,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (kt + 2 == nt) mma_commit(bar(BAR_QEMPTY + t));  // last S_t of the unit
                         }
                         __syncwarp();
-                        if (t == 0) ++sc0; else ++sc1;
                     }
                 }
                 if (!ok) break;
@@ -570,12 +579,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
             }
         }
+        *mma_exit = 1;  // the release warp may stop
         // every MMA this warp issued has completed before tensor memory is freed
         if (elect_one()) {
             mma_commit(bar(BAR_MMADONE));
             drain_bounded(bar(BAR_MMADONE), 0, limit);
         }
         __syncwarp();
+      } else if (warp == kReleaseWarp) {
+        // =========================== release warp ===========================
+        // Sleeps until the MMA warp leaves its loop; if the abort flag goes up first,
+        // it arrives on every P barrier (as the softmax warps would) so that an MMA
+        // warp waiting there moves on, sees the abort at its next bounded wait and
+        // leaves.  Surplus arrivals only complete generations nobody waits for.
+        const unsigned long long cap = 64ull * limit;
+        unsigned long long i = 0;
+        for (; i < cap && !*mma_exit; ++i) {
+            if (*abort_flag) {
+                for (int b = 0; b < 2 * kTiles; ++b)
+                    for (int k = 0; k < 4; ++k) named_bar_arrive(kBarP + b, kBarPThreads);
+            } else {
+                nanosleep_ns(1024);
+            }
+        }
+        if (i == cap) atomicOr(&g_attn_status, kStatusTimeout);
       }
     } else if (wg < 2) {
         // =========================== softmax warpgroups =====================
@@ -696,7 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tmem_wait_st();
                     tc_fence_before();
-                    mbar_arrive(bar(BAR_PFULL + 2 * t + h));
+                    named_bar_arrive(kBarP + 2 * t + h, kBarPThreads);
                 }
                 l_run = l_run * alpha + ((rs0 + rs1) + (rs2 + rs3));
             }

@@ -145,6 +145,15 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Arrive without waiting: counts the warp's 32 threads toward the barrier's nthreads.
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ void nanosleep_ns(uint32_t ns) {
+    asm volatile("nanosleep.u32 %0;" ::"r"(ns));
+}
+
 // ------------------------------------------------------------------ tcgen05: TMEM
 // Allocation is warp-wide; the base address is written to shared memory.
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
