@@ -26,7 +26,11 @@
 //
 // Warp roles (320 threads): warps 0-7 elementwise work (warp w owns TMEM lane
 // quarter w % 4 and one half of the 128 columns: w / 4), warp 8 issues the MMAs
-// (one elected lane), warp 9 drives the TMA copies.  The operand that stays
+// (one elected lane), warp 9 drives the TMA copies and then serves as the release
+// warp of the abort path.  The elementwise warps hand P and dS to the MMA warp
+// through hardware named barriers (they arrive, it syncs), as in the forward
+// kernel: an mbarrier poll by the MMA-issuing warp would first wait for its
+// queued MMAs to drain.  The operand that stays
 // fixed for the CTA (K and V, or Q and dO) is loaded once; the other pair
 // streams through a two-stage ring.  Every mbarrier wait is bounded as in the
 // forward kernel (timeout status, CTA abort flag, drained copies, freed TMEM).
@@ -39,6 +43,30 @@
 namespace attn {
 namespace bwd {
 
+// The release loop of the abort path, run by a whole warp (the forward kernel's
+// release warp does the same inline).  An MMA warp that waits on a hardware named
+// barrier cannot time out, so until that warp reports (through mma_exit) that it
+// left its loop, this loop sleeps; once the abort flag is up it arrives on the
+// named barriers first_id .. first_id + n_ids - 1, arrivals_per_round times each
+// per round (the other parties' share of nthreads), so a waiting MMA warp moves on
+// and meets the abort at its next bounded mbarrier wait.  Surplus arrivals only
+// complete generations nobody waits for.
+__device__ __forceinline__ void release_named_barriers(volatile int* mma_exit, volatile int* abort_flag,
+                                                       uint32_t first_id, int n_ids, uint32_t nthreads,
+                                                       int arrivals_per_round, unsigned int limit) {
+    const unsigned long long cap = 64ull * limit;
+    unsigned long long i = 0;
+    for (; i < cap && !*mma_exit; ++i) {
+        if (*abort_flag) {
+            for (int b = 0; b < n_ids; ++b)
+                for (int k = 0; k < arrivals_per_round; ++k) named_bar_arrive(first_id + b, nthreads);
+        } else {
+            nanosleep_ns(1024);
+        }
+    }
+    if (i == cap) atomicOr(&g_attn_status, kStatusTimeout);
+}
+
 // The elementwise warps split each 128-column tile into kGroups groups of
 // kCols columns: warp w owns TMEM lane quarter w % 4 and column group w / 4.
 constexpr int kGroups = 2;
@@ -49,6 +77,10 @@ constexpr int kLoadWarp = kComputeWarps + 1;
 constexpr int kThreads = 32 * (kComputeWarps + 2);
 constexpr int kStages = 2;
 constexpr int kVecBytes = kBM * 4;  // lse2 or delta of one 128-row tile
+// named barriers (elementwise warps arrive, the MMA warp syncs): P (or S read out)
+// and dS in tensor memory
+constexpr uint32_t kBarPReady = 2, kBarDsReady = 3;
+constexpr uint32_t kBarReadyThreads = 32 * kComputeWarps + 32;
 
 // Barriers of the dK/dV kernel.
 enum : int {
@@ -60,8 +92,6 @@ enum : int {
     BAR_EMPTY = BAR_FULL + kStages,
     BAR_SFULL = BAR_EMPTY + kStages,
     BAR_DPFULL,
-    BAR_PREADY,                    // P^T in tensor memory (256 arrivals)
-    BAR_DSREADY,                   // dS^T in tensor memory (256 arrivals)
     BAR_ACCDONE,                   // the item's last dK completed
     BAR_ITEMFULL,                  // [2] next work item published
     BAR_ITEMEMPTY = BAR_ITEMFULL + 2,  // [2] read by the MMA warp and the 8 elementwise warps
@@ -85,7 +115,8 @@ struct BwdGeo {
     static constexpr int kTmemSlot = kBar + BAR_COUNT * 8;
     static constexpr int kAbort = kTmemSlot + 4;
     static constexpr int kItems = kAbort + 4;          // [2] published work items
-    static constexpr int kSmemBytes = kItems + 8 + 1024;
+    static constexpr int kMmaExit = kItems + 8;        // set once the MMA warp left its loop
+    static constexpr int kSmemBytes = kMmaExit + 4 + 1024;
     static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
     // tensor-memory columns
     static constexpr uint32_t kTmemS = 0;
@@ -366,6 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = static_cast<int>(threadIdx.x) & 31;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + G::kAbort);
     volatile int* item_slot = reinterpret_cast<volatile int*>(smem + G::kItems);
+    volatile int* mma_exit = reinterpret_cast<volatile int*>(smem + G::kMmaExit);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::kTmemSlot);
     auto bar = [&](int i) -> uint32_t { return sbase + G::kBar + 8 * i; };
     const int n_items = p.B * p.Hkv * p.n_kv_tiles;
@@ -390,8 +422,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(bar(BAR_SFULL), 1);
         mbar_init(bar(BAR_DPFULL), 1);
-        mbar_init(bar(BAR_PREADY), 32 * kComputeWarps);
-        mbar_init(bar(BAR_DSREADY), 32 * kComputeWarps);
         mbar_init(bar(BAR_ACCDONE), 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(BAR_ITEMFULL + i), 1);
@@ -399,6 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(bar(BAR_MMADONE), 1);
         *abort_flag = 0;
+        *mma_exit = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_do);
@@ -480,6 +511,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
+        // release warp of the abort path: the elementwise warps' arrivals
+        release_named_barriers(mma_exit, abort_flag, kBarPReady, 2, kBarReadyThreads, kComputeWarps, limit);
     } else if (warp == kMmaWarp) {
         // =========================== MMA issuer =============================
         constexpr uint32_t idesc_s = idesc_f16kind_f32(kBN, kBM, false, kF16);  // S^T, dP^T
@@ -544,10 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (steps == 1) commit_to(BAR_VEMPTY);
             for (int st = 0; ok && st < steps; ++st) {
                 const int gs = g + st;
-                if (!wait_bounded(bar(BAR_PREADY), gs & 1, abort_flag, limit)) {
-                    ok = false;
-                    break;
-                }
+                named_bar_sync(kBarPReady, kBarReadyThreads);  // P^T_st in tensor memory
                 tc_fence_after();
                 if (elect_one()) mma_tmem_mn(tDV, tS, do_mn0 + stage_off(gs), idesc_acc, st > 0);
                 __syncwarp();
@@ -558,10 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (st + 2 == steps) commit_to(BAR_KEMPTY);  // the item's last S^T is issued
                 }
-                if (!wait_bounded(bar(BAR_DSREADY), gs & 1, abort_flag, limit)) {
-                    ok = false;
-                    break;
-                }
+                named_bar_sync(kBarDsReady, kBarReadyThreads);  // dS^T_st in tensor memory
                 tc_fence_after();
                 if (elect_one()) {
                     mma_tmem_mn(tDK, tDP, q_mn0 + stage_off(gs), idesc_acc, st > 0);
@@ -577,6 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             g += steps;
             ++w;
         }
+        *mma_exit = 1;  // the release loop may stop
         if (elect_one()) {
             mma_commit(bar(BAR_MMADONE));
             drain_bounded(bar(BAR_MMADONE), 0, limit);
@@ -646,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(bar(BAR_PREADY));
+                named_bar_arrive(kBarPReady, kBarReadyThreads);
                 const bool got2 = wait_bounded(bar(BAR_DPFULL), gs & 1, abort_flag, limit);
                 if (!__all_sync(0xffffffffu, got2)) {
                     ok = false;
@@ -667,12 +695,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(bar(BAR_DSREADY));
+                named_bar_arrive(kBarDsReady, kBarReadyThreads);
             }
             if (!ok) break;
             // epilogue: dV and scale * dK of this key, columns [grp kD/kGroups, (grp+1) kD/kGroups).
             // The accumulators are read out (tcgen05.ld completed) before this
-            // thread's next PREADY, which gates the next item's first dV and dK.
+            // thread's next arrival on the P barrier, which gates the next item's
+            // first dV and dK.
             bool have = steps > 0;
             if (have) {
                 const bool got = wait_bounded(bar(BAR_ACCDONE), w & 1, abort_flag, limit);
@@ -719,7 +748,8 @@ struct DqGeo {
     static constexpr int kTmemSlot = kBar + 24 * 8;
     static constexpr int kAbort = kTmemSlot + 4;
     static constexpr int kItems = kAbort + 4;          // [2] published work items
-    static constexpr int kSmemBytes = kItems + 8 + 1024;
+    static constexpr int kMmaExit = kItems + 8;        // set once the MMA warp left its loop
+    static constexpr int kSmemBytes = kMmaExit + 4 + 1024;
     static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
     static constexpr uint32_t kTmemS = 0, kTmemDP = 128, kTmemDQ = 256;
 };
@@ -735,8 +765,6 @@ enum : int {
     DQB_VEMPTY = DQB_VFULL + 2,
     DQB_SFULL = DQB_VEMPTY + 2,
     DQB_DPFULL,
-    DQB_PREADY,           // S_n read out of tensor memory (256 arrivals)
-    DQB_DSREADY,          // dS_n in tensor memory (256 arrivals)
     DQB_ACCDONE,          // the item's last dQ product completed
     DQB_ITEMFULL,         // [2]
     DQB_ITEMEMPTY = DQB_ITEMFULL + 2,  // [2]
@@ -779,6 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = static_cast<int>(threadIdx.x) & 31;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + G::kAbort);
     volatile int* item_slot = reinterpret_cast<volatile int*>(smem + G::kItems);
+    volatile int* mma_exit = reinterpret_cast<volatile int*>(smem + G::kMmaExit);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::kTmemSlot);
     auto bar = [&](int i) -> uint32_t { return sbase + G::kBar + 8 * i; };
     const int n_items = p.B * p.Hq * p.n_q_tiles;
@@ -799,8 +828,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(bar(DQB_SFULL), 1);
         mbar_init(bar(DQB_DPFULL), 1);
-        mbar_init(bar(DQB_PREADY), 32 * kComputeWarps);
-        mbar_init(bar(DQB_DSREADY), 32 * kComputeWarps);
         mbar_init(bar(DQB_ACCDONE), 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(DQB_ITEMFULL + i), 1);
@@ -808,6 +835,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(bar(DQB_MMADONE), 1);
         *abort_flag = 0;
+        *mma_exit = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_do);
@@ -895,6 +923,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
+        // release warp of the abort path: the elementwise warps' arrivals
+        release_named_barriers(mma_exit, abort_flag, kBarPReady, 2, kBarReadyThreads, kComputeWarps, limit);
     } else if (warp == kMmaWarp) {
         // =========================== MMA issuer =============================
         constexpr uint32_t idesc_s = idesc_f16kind_f32(kBM, kBN, false, kF16);  // S, dP
@@ -908,11 +938,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tDQ = tmem_base + G::kTmemDQ;
         // Per item, issue order S_0, dP_0, then per KV tile n:
         //   [S_n read out] S_{n+1}, [dS_n stored] dQ_n, dP_{n+1}
-        // The elementwise warps signal (PREADY) as soon as S_n is in their
+        // The elementwise warps signal (P barrier) as soon as S_n is in their
         // registers, so S_{n+1} runs while they form P_n and dS_n; dP_{n+1}
         // overwrites dS_n only after dQ_n (issue order).  A V stage is released
         // right after its dP, a K stage after its dQ.  g counts KV steps over all
-        // items; PREADY is awaited on every step, including an item's last, so
+        // items; the P barrier is met on every step, including an item's last, so
         // the next item's S_0 never overwrites an S still being read.
         auto issue_s = [&](int gk) -> bool {  // S of global KV step gk; its K must have landed
             const int ks = gk % G::kKStages;
@@ -956,7 +986,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nkv = kv_tiles_for_rows(p, t * kBM);
             if (nkv == 0) continue;
             // the previous item's last S must have been read out before S_0 overwrites it
-            if (g > 0 && !wait_bounded(bar(DQB_PREADY), (g - 1) & 1, abort_flag, limit)) break;
+            if (g > 0) named_bar_sync(kBarPReady, kBarReadyThreads);
             ok = wait_bounded(bar(DQB_QFULL), w & 1, abort_flag, limit) && issue_s(g);
             if (!ok) break;
             if (nkv == 1) commit_to(DQB_QEMPTY);
@@ -968,16 +998,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int ks = gk % G::kKStages;
                 const uint64_t so = static_cast<uint64_t>((ks * G::kTileBytes) >> 4);
                 if (kt + 1 < nkv) {
-                    if (!wait_bounded(bar(DQB_PREADY), gk & 1, abort_flag, limit) || !issue_s(gk + 1)) {
+                    named_bar_sync(kBarPReady, kBarReadyThreads);  // S_kt read out of tensor memory
+                    if (!issue_s(gk + 1)) {
                         ok = false;
                         break;
                     }
                     if (kt + 2 == nkv) commit_to(DQB_QEMPTY);  // the item's last S is issued
                 }
-                if (!wait_bounded(bar(DQB_DSREADY), gk & 1, abort_flag, limit)) {
-                    ok = false;
-                    break;
-                }
+                named_bar_sync(kBarDsReady, kBarReadyThreads);  // dS_kt in tensor memory
                 tc_fence_after();
                 if (elect_one()) {
                     mma_tmem_mn(tDQ, tDP, k_mn0 + so, idesc_acc, kt > 0);
@@ -996,6 +1024,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             g += nkv;
             ++w;
         }
+        // the last item's last S read-out is the one signal not yet met (each
+        // other one is met before the S that follows it)
+        if (ok && g > 0) named_bar_sync(kBarPReady, kBarReadyThreads);
+        *mma_exit = 1;  // the release loop may stop
         if (elect_one()) {
             mma_commit(bar(DQB_MMADONE));
             drain_bounded(bar(DQB_MMADONE), 0, limit);
@@ -1042,7 +1074,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t x[kCols];
                 tmem_ld_cols<kCols>(tS, x);
                 tc_fence_before();
-                mbar_arrive(bar(DQB_PREADY));  // S may now be overwritten by the next tile's product
+                named_bar_arrive(kBarPReady, kBarReadyThreads);  // S may now be overwritten by the next tile's product
                 float pv[kCols];
 #pragma unroll
                 for (int c = 0; c < kCols; c += 2) {
@@ -1076,11 +1108,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(bar(DQB_DSREADY));
+                named_bar_arrive(kBarDsReady, kBarReadyThreads);
             }
             if (!ok) break;
             // epilogue: scale * dQ of this row, columns [grp kD/kGroups, (grp+1) kD/kGroups); the
-            // accumulator is read out before this thread's next DSREADY, which gates
+            // accumulator is read out before this thread's next dS-barrier arrival, which gates
             // the next item's first dQ product
             const bool have = nkv > 0;
             if (have) {
