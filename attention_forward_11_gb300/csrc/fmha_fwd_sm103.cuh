@@ -3,9 +3,11 @@
 // Work unit = two 128-row query tiles that read the same K/V head: either two
 // consecutive row tiles of one query head, or (when the GQA group has an even
 // number of query heads) the same rows of two query heads of one group, so
-// every K/V tile brought into shared memory feeds 256 query rows.  Units are
-// numbered longest first (causal row tiles near the end of the sequence visit
-// the most KV tiles -- the Choreo tutorial's non-persistent schedule); a
+// every K/V tile brought into shared memory feeds 256 query rows.  Under a causal
+// mask units are numbered longest first (row tiles near the end of the sequence
+// visit the most KV tiles -- the Choreo tutorial's non-persistent schedule);
+// without one every unit is equally long and they are numbered head-major, so
+// the units of one K/V head run side by side and its K and V stay in L2; a
 // persistent grid of at most one CTA per SM takes them in a snake order
 // (round r: CTA c takes unit r*G + c, or r*G + G-1-c on odd rounds), so the
 // next unit's Q is loaded while the current one finishes.
@@ -224,9 +226,18 @@ struct Unit {
 
 __host__ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
     Unit w;
-    const int inner_count = p.B * p.n_head_units;
-    const int ru = u / inner_count;
-    const int inner = u % inner_count;
+    int ru, inner;
+    if (p.causal) {
+        // longest first: row units outermost (descending), then batch and head unit
+        const int inner_count = p.B * p.n_head_units;
+        ru = u / inner_count;
+        inner = u % inner_count;
+    } else {
+        // every unit visits every KV tile: head-major, so the units of one K/V head
+        // run side by side and its K and V stay in L2
+        ru = u % p.n_row_units;
+        inner = u / p.n_row_units;
+    }
     w.b = inner / p.n_head_units;
     const int hu = inner % p.n_head_units;
     const int row_unit = p.causal ? (p.n_row_units - 1 - ru) : ru;
