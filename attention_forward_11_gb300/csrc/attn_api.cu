@@ -90,6 +90,7 @@ bool device_setup(int dev, int* sm_count) {
         if (!opt_in_smem<attn::PlainSched, false, 128>() || !opt_in_smem<attn::PlainSched, true, 128>() ||
             !opt_in_smem<attn::SplitSched, false, 128>() || !opt_in_smem<attn::PlainSched, false, 64>() ||
             !opt_in_smem<attn::PlainSched, true, 64>() || !opt_in_smem<attn::SplitSched, false, 64>() ||
+            !opt_in_smem<attn::TableSched, false, 128>() || !opt_in_smem<attn::TableSched, true, 128>() ||
             !opt_in_smem_bwd<false, 128>() || !opt_in_smem_bwd<true, 128>() || !opt_in_smem_bwd<false, 64>() ||
             !opt_in_smem_bwd<true, 64>() ||
             cudaFuncSetAttribute(attn::d256::fmha_fwd_d256_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -295,6 +296,83 @@ void build_split_plan(const attn::FwdParams& p, int sms, SplitPlan* plan) {
     plan->split = true;
 }
 
+// The whole-unit schedule's table for causal shapes (TableSched): units in blocks
+// of K/V heads whose K and V together take at most kTableBlockBytes, longest first
+// within a block; each unit in turn goes to the least-loaded CTA (its KV tiles
+// plus one for the unit's own start-up), which keeps the CTAs' totals within a
+// unit of each other while a block's heads run side by side and their K and V
+// stay in L2.  Returns false where the snake order is used instead: unmasked
+// shapes (already numbered head-major) and shapes beyond the table's size.
+constexpr long long kTableBlockBytes = 48ll << 20;
+bool build_plain_table(const attn::FwdParams& p, int grid, attn::TableSched* sc) {
+    if (!p.causal || p.n_units > attn::kMaxTable || grid < 1 || grid > attn::kMaxSplitCtas) return false;
+    const int inner_count = p.B * p.n_head_units;              // (batch, head unit) pairs
+    const int units_per_kv = p.n_head_units / p.Hkv > 0 ? p.n_head_units / p.Hkv : 1;
+    const long long kv_bytes = 4ll * p.Skv * p.D;               // K and V of one K/V head
+    const long long kv_per_block = std::max<long long>(1, kTableBlockBytes / std::max<long long>(1, kv_bytes));
+    const int block = static_cast<int>(std::min<long long>(inner_count, kv_per_block * units_per_kv));
+    long long load[attn::kMaxSplitCtas] = {};
+    unsigned short count[attn::kMaxSplitCtas] = {};
+    unsigned short owner[attn::kMaxTable];
+    unsigned short order[attn::kMaxTable];
+    int n = 0;
+    for (int s = 0; s < inner_count; s += block)
+        for (int ru = 0; ru < p.n_row_units; ++ru)
+            for (int inner = s; inner < std::min(inner_count, s + block); ++inner) {
+                const int u = ru * inner_count + inner;
+                int c = 0;
+                for (int k = 1; k < grid; ++k)
+                    if (load[k] < load[c]) c = k;
+                load[c] += attn::decode_unit(p, u).nmax() + 1;
+                owner[n] = static_cast<unsigned short>(c);
+                order[n] = static_cast<unsigned short>(u);
+                ++count[c];
+                ++n;
+            }
+    if (n != p.n_units) return false;
+    int pos = 0;
+    for (int c = 0; c < grid; ++c) {
+        sc->cta_begin[c] = static_cast<unsigned short>(pos);
+        pos += count[c];
+    }
+    sc->cta_begin[grid] = static_cast<unsigned short>(pos);
+    unsigned short fill[attn::kMaxSplitCtas] = {};
+    for (int i = 0; i < n; ++i) {  // each CTA's units in the order they were handed out
+        const int c = owner[i];
+        sc->unit[sc->cta_begin[c] + fill[c]++] = order[i];
+    }
+    return true;
+}
+
+// build_plain_table for the last few shapes, so a repeated call costs a copy
+// (the greedy assignment takes ~units x CTAs steps on the host)
+bool plain_table_cached(const attn::FwdParams& p, int grid, attn::TableSched* out) {
+    struct Entry {
+        int key[9];
+        bool ok;
+        attn::TableSched sched;
+    };
+    constexpr int kEntries = 8;
+    static Entry cache[kEntries];
+    static int used = 0, next = 0;
+    static std::mutex mu;
+    const int key[9] = {p.B, p.Sq, p.Skv, p.Hq, p.Hkv, p.D, p.causal, grid, p.n_units};
+    std::lock_guard<std::mutex> lock(mu);
+    for (int e = 0; e < used; ++e)
+        if (std::memcmp(cache[e].key, key, sizeof(key)) == 0) {
+            if (cache[e].ok) std::memcpy(out, &cache[e].sched, sizeof(*out));
+            return cache[e].ok;
+        }
+    const bool ok = build_plain_table(p, grid, out);
+    Entry& slot = cache[next];
+    std::memcpy(slot.key, key, sizeof(key));
+    slot.ok = ok;
+    if (ok) std::memcpy(&slot.sched, out, sizeof(*out));
+    next = (next + 1) % kEntries;
+    if (used < kEntries) ++used;
+    return ok;
+}
+
 template <bool kF16 = false>
 attn_status_t launch_plain(const CUtensorMap* tm, const attn::FwdParams& p, int sms, cudaStream_t stream) {
     if (p.D == 256) {
@@ -309,10 +387,15 @@ attn_status_t launch_plain(const CUtensorMap* tm, const attn::FwdParams& p, int 
     }
     // persistent grid: at most one CTA per SM (the CTA holds all 512 TMEM columns)
     const int grid = p.n_units < sms ? p.n_units : sms;
+    static thread_local attn::TableSched table;  // 4.6 KB: kept off the stack
     if (p.D == 64)
         attn::fmha_fwd_kernel<attn::PlainSched, kF16, 64><<<static_cast<unsigned int>(grid), attn::kThreads,
                                                             attn::Geo<64>::kSmemBytes, stream>>>(
             tm[0], tm[1], tm[2], tm[3], p, attn::PlainSched{0});
+    else if (plain_table_cached(p, grid, &table))  // head size 128, causal: the head-blocked table
+        attn::fmha_fwd_kernel<attn::TableSched, kF16, 128><<<static_cast<unsigned int>(grid), attn::kThreads,
+                                                             attn::Geo<128>::kSmemBytes, stream>>>(
+            tm[0], tm[1], tm[2], tm[3], p, table);
     else
         attn::fmha_fwd_kernel<attn::PlainSched, kF16, 128><<<static_cast<unsigned int>(grid), attn::kThreads,
                                                              attn::Geo<128>::kSmemBytes, stream>>>(

@@ -267,9 +267,21 @@ __device__ __forceinline__ int unit_of(const FwdParams& p, int j) {
 }
 
 // ---- schedules of work items over the persistent grid
-// Whole units, longest first, in the snake order of unit_of().
+constexpr int kMaxSplitCtas = 256;
+// Whole units in the order above, in the snake order of unit_of().
 struct PlainSched {
     int unused;
+};
+// Whole units from a table (causal shapes of up to kMaxTable units): per CTA, the
+// units the host assigned to it, in the order it takes them.  The host orders
+// the units in blocks of heads whose K and V together fit in part of L2, longest
+// first within each block, and hands each unit in turn to the least-loaded CTA,
+// so the heads of one block run side by side (their K and V are read from DRAM
+// about once) and the CTAs still finish together.
+constexpr int kMaxTable = 2048;
+struct TableSched {
+    unsigned short cta_begin[kMaxSplitCtas + 1];
+    unsigned short unit[kMaxTable];
 };
 
 // Split-KV: the host cuts the sequence of (unit, KV tile) iterations into equal
@@ -282,7 +294,6 @@ struct Piece {
     int slot;             // workspace slot, or -1 for a whole unit
 };
 constexpr int kMaxPieces = 1024;
-constexpr int kMaxSplitCtas = 256;
 struct SplitSched {
     float* ws_o;          // [slot][tile][row][D] fp32 raw accumulators
     float2* ws_ml;        // [slot][tile][row] (running max in log2 units, row sum)
@@ -295,6 +306,13 @@ __device__ __forceinline__ bool get_work(const FwdParams& p, const PlainSched&, 
     const int u = unit_of(p, j);
     if (u < 0) return false;
     w = decode_unit(p, u);
+    return true;
+}
+
+__device__ __forceinline__ bool get_work(const FwdParams& p, const TableSched& sc, int j, Unit& w) {
+    const int i = sc.cta_begin[blockIdx.x] + j;
+    if (i >= sc.cta_begin[blockIdx.x + 1]) return false;
+    w = decode_unit(p, sc.unit[i]);
     return true;
 }
 
