@@ -26,7 +26,7 @@ EXPORTED = ("attn_fwd", "attn_fwd_ex", "attn_fwd_splitkv", "attn_fwd_splitkv_wor
             "attn_fwd_splitkv_noalloc", "attn_status_str", "attn_last_device_status",
             "attn_check_device_status",
             "attn_kernel_launches", "attn_debug_wait_timeout", "attn_bwd", "attn_bwd_workspace_size",
-            "attn_debug_unit_rates")
+            "attn_debug_unit_rates", "attn_debug_unit_schedule")
 
 _lock = threading.Lock()
 _lib = None
@@ -75,6 +75,9 @@ def load_library():
         lib.attn_debug_wait_timeout.restype = I
         lib.attn_debug_unit_rates.argtypes = [ctypes.POINTER(ctypes.c_double), I, P]
         lib.attn_debug_unit_rates.restype = I
+        IP = ctypes.POINTER(ctypes.c_int)
+        lib.attn_debug_unit_schedule.argtypes = [I, I, I, I, I, I, I, I, IP, IP, I, IP]
+        lib.attn_debug_unit_schedule.restype = I
         lib.attn_fwd_splitkv_workspace_size.argtypes = [I, I, I, I, I, I, I,
                                                         ctypes.POINTER(ctypes.c_size_t)]
         lib.attn_fwd_splitkv_workspace_size.restype = I
@@ -308,3 +311,20 @@ def attn_debug_unit_rates(stream=None) -> dict:
     if st != ATTN_OK:
         raise AttnError(st, "attn_debug_unit_rates")
     return dict(zip(UNIT_RATE_NAMES, list(out)))
+
+
+def attn_debug_unit_schedule(B: int, Sq: int, Skv: int, Hq: int, Hkv: int, D: int, causal: int, sms: int):
+    """The forward's unit table for a shape on `sms` SMs (host only): (cta_begin,
+    units) as lists, or None when the snake order is used instead."""
+    grid_cap, cap = 257, 1 << 16
+    cta_begin = (ctypes.c_int * grid_cap)()
+    units = (ctypes.c_int * cap)()
+    n = ctypes.c_int(-1)
+    st = load_library().attn_debug_unit_schedule(int(B), int(Sq), int(Skv), int(Hq), int(Hkv), int(D), int(causal),
+                                                 int(sms), cta_begin, units, cap, ctypes.byref(n))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_debug_unit_schedule")
+    if n.value == 0:
+        return None
+    grid = min(sms, n.value)
+    return list(cta_begin[:grid + 1]), list(units[:n.value])

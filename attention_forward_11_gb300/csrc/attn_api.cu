@@ -771,6 +771,27 @@ attn_status_t run_mma_rate(int sms, cudaStream_t stream, double* clocks_per_mma)
 }
 }  // namespace
 
+extern "C" attn_status_t attn_debug_unit_schedule(int B, int Sq, int Skv, int Hq, int Hkv, int D, int causal,
+                                                   int sms, int* cta_begin, int* units, int cap, int* n_units_out) {
+    const attn_status_t sz = check_sizes(B, Sq, Skv, Hq, Hkv, D, causal);
+    if (sz != ATTN_OK) return sz;
+    if (sms < 1 || sms > attn::kMaxSplitCtas || !cta_begin || !units || !n_units_out) return ATTN_ERR_INVALID_ARG;
+    attn::FwdParams p;
+    static int dummy_o;
+    const attn_status_t pr = make_params(B, Sq, Skv, Hq, Hkv, causal, 1.0f, &dummy_o, nullptr, &p, D);
+    if (pr != ATTN_OK) return pr;
+    *n_units_out = 0;
+    if (D != 128) return ATTN_OK;  // head size 64 keeps the snake order; 256 runs its own kernel
+    const int grid = p.n_units < sms ? p.n_units : sms;
+    attn::TableSched table;
+    if (!build_plain_table(p, grid, &table)) return ATTN_OK;
+    if (cap < p.n_units) return ATTN_ERR_INVALID_ARG;
+    for (int c = 0; c <= grid; ++c) cta_begin[c] = table.cta_begin[c];
+    for (int i = 0; i < p.n_units; ++i) units[i] = table.unit[i];
+    *n_units_out = p.n_units;
+    return ATTN_OK;
+}
+
 extern "C" attn_status_t attn_debug_unit_rates(double* out, int n, cudaStream_t stream) {
     if (out == nullptr || n < ATTN_UNIT_RATES) return ATTN_ERR_INVALID_ARG;
     int dev = 0, sms = 0;

@@ -249,6 +249,28 @@ attn_status_t attn_debug_wait_timeout(unsigned int poll_limit, cudaStream_t stre
 #define ATTN_UNIT_RATES 8
 attn_status_t attn_debug_unit_rates(double* out, int n, cudaStream_t stream);
 
+/*
+ * The forward's unit schedule for a shape (diagnostic; host only, launches
+ * nothing).  attn_fwd runs two 128-row query tiles per work unit on a
+ * persistent grid of min(#units, sms) CTAs.  For causal shapes of head size
+ * 128 with at most 2048 units it takes the units from a table: the units in
+ * blocks of heads whose K and V together take at most 48 MB, longest first
+ * within a block, each unit handed to the least-loaded CTA.  Otherwise each
+ * CTA takes units in a snake order and no table exists.
+ *   sms          number of SMs to plan for, in [1, 256]
+ *   cta_begin    (host, >= grid + 1 ints, grid = min(#units, sms)) receives
+ *                the table's per-CTA start offsets into `units`
+ *   units        (host, `cap` ints) receives the unit indices, CTA after CTA,
+ *                each CTA's in the order it takes them
+ *   n_units_out  receives the number of units in the table, or 0 when the
+ *                snake order is used (cta_begin and units are then untouched)
+ * Returns ATTN_ERR_INVALID_ARG for invalid sizes, sms out of range, a NULL
+ * pointer, or a `cap` smaller than the table; ATTN_ERR_UNSUPPORTED for a head
+ * size other than 64, 128 or 256; else ATTN_OK.
+ */
+attn_status_t attn_debug_unit_schedule(int B, int Sq, int Skv, int Hq, int Hkv, int D, int causal, int sms,
+                                       int* cta_begin, int* units, int cap, int* n_units_out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -218,3 +218,93 @@ def test_unit_rates_arguments_checked_before_any_launch(lib):
     out = (ctypes.c_double * 8)()
     assert lib.attn_debug_unit_rates(None, 8, None) == fa.ATTN_ERR_INVALID_ARG
     assert lib.attn_debug_unit_rates(out, 7, None) == fa.ATTN_ERR_INVALID_ARG
+
+
+# ---- the forward's unit table (host logic; no GPU)
+def _kv_tiles(row0, Sq, Skv, causal):
+    """KV tiles a 128-row query tile starting at row0 visits (key j visible from
+    row i iff j <= i + diag; diag = Skv - Sq bottom-right, 0 top-left)."""
+    if row0 >= Sq:
+        return 0
+    n_all = -(-Skv // 128)
+    if not causal:
+        return n_all
+    diag = Skv - Sq if causal == 1 else 0
+    last_key = min(row0 + 127, Sq - 1) + diag
+    return 0 if last_key < 0 else min(n_all, last_key // 128 + 1)
+
+
+def _unit_weights(B, Sq, Skv, Hq, Hkv, causal):
+    """KV steps of every unit in the forward's causal numbering: row units
+    outermost (longest first), then batch and head unit; a unit is two row
+    tiles of one head, or one row tile of two heads when the group is even."""
+    pairs = (Hq // Hkv) % 2 == 0
+    n_head_units = Hq // 2 if pairs else Hq
+    rows_per_unit = 128 if pairs else 256
+    n_row_units = -(-Sq // rows_per_unit)
+    w = []
+    for ru in range(n_row_units):
+        row_unit = n_row_units - 1 - ru
+        for _ in range(B * n_head_units):
+            if pairs:
+                r0 = r1 = row_unit * 128
+            else:
+                r0, r1 = row_unit * 256, row_unit * 256 + 128
+            w.append(max(_kv_tiles(r0, Sq, Skv, causal), _kv_tiles(r1, Sq, Skv, causal)))
+    return w, B * n_head_units
+
+
+@pytest.mark.parametrize("shape", [(4, 4096, 4096, 16, 16, 1), (2, 8192, 8192, 32, 8, 1), (1, 2048, 3000, 8, 8, 1),
+                                   (3, 1000, 1000, 6, 3, 2), (1, 512, 32768, 64, 8, 1)])
+def test_unit_table_is_a_balanced_permutation(shape):
+    B, Sq, Skv, Hq, Hkv, causal = shape
+    sms = 152
+    table = fa.attn_debug_unit_schedule(B, Sq, Skv, Hq, Hkv, 128, causal, sms)
+    weights, inner_count = _unit_weights(B, Sq, Skv, Hq, Hkv, causal)
+    assert table is not None
+    cta_begin, units = table
+    n = len(weights)
+    grid = min(n, sms)
+    assert len(cta_begin) == grid + 1 and cta_begin[0] == 0 and cta_begin[-1] == n
+    assert all(a <= b for a, b in zip(cta_begin, cta_begin[1:]))
+    assert sorted(units) == list(range(n)), "every unit exactly once"
+    # each unit went to the least-loaded CTA: the CTAs' totals (KV steps plus one
+    # per unit) differ by at most the heaviest unit
+    loads = [sum(weights[u] + 1 for u in units[cta_begin[c]:cta_begin[c + 1]]) for c in range(grid)]
+    assert max(loads) - min(loads) <= max(weights) + 1
+    # within a CTA the units come in the table's order: blocks of heads whose K
+    # and V take at most 48 MB, in turn, longest first inside each block
+    units_per_kv = max(1, inner_count // B // Hkv)
+    per_block = min(inner_count, max(1, (48 << 20) // (4 * Skv * 128)) * units_per_kv)
+    block_of = lambda u: (u % inner_count) // per_block
+    for c in range(grid):
+        mine = units[cta_begin[c]:cta_begin[c + 1]]
+        assert [block_of(u) for u in mine] == sorted(block_of(u) for u in mine)
+        for a, b in zip(mine, mine[1:]):
+            if block_of(a) == block_of(b):
+                assert weights[a] >= weights[b]
+
+
+def test_unit_table_only_for_causal_head_size_128_up_to_its_size():
+    assert fa.attn_debug_unit_schedule(1, 16384, 16384, 16, 16, 128, 0, 152) is None   # unmasked: head-major
+    assert fa.attn_debug_unit_schedule(4, 4096, 4096, 16, 16, 64, 1, 152) is None     # head size 64: snake
+    assert fa.attn_debug_unit_schedule(4, 4096, 4096, 16, 16, 256, 1, 152) is None    # own kernel
+    assert fa.attn_debug_unit_schedule(16, 8192, 8192, 32, 32, 128, 1, 152) is None  # 8192 units > 2048
+
+
+def test_unit_table_rejects_bad_arguments():
+    lib = fa.load_library()
+    n = ctypes.c_int(0)
+    buf = (ctypes.c_int * 4096)()
+    beg = (ctypes.c_int * 300)()
+    for sms in (0, 257):
+        assert lib.attn_debug_unit_schedule(4, 4096, 4096, 16, 16, 128, 1, sms, beg, buf, 4096,
+                                            ctypes.byref(n)) == fa.ATTN_ERR_INVALID_ARG
+    assert lib.attn_debug_unit_schedule(4, 4096, 4096, 16, 16, 128, 1, 152, None, buf, 4096,
+                                        ctypes.byref(n)) == fa.ATTN_ERR_INVALID_ARG
+    assert lib.attn_debug_unit_schedule(4, 4096, 4096, 16, 16, 128, 1, 152, beg, buf, 1000,
+                                        ctypes.byref(n)) == fa.ATTN_ERR_INVALID_ARG   # 1024 units
+    assert lib.attn_debug_unit_schedule(4, 4096, 4096, 15, 4, 128, 1, 152, beg, buf, 4096,
+                                        ctypes.byref(n)) == fa.ATTN_ERR_INVALID_ARG   # Hq % Hkv
+    assert lib.attn_debug_unit_schedule(4, 4096, 4096, 16, 16, 96, 1, 152, beg, buf, 4096,
+                                        ctypes.byref(n)) == fa.ATTN_ERR_UNSUPPORTED
