@@ -9,7 +9,9 @@ stream, inputs resident in HBM, L2 flushed (a 256 MiB write) between steps.
 `e2e` is the same metric through the C ABI with pinned host buffers: the
 host->device copies of Q, K, V and the device->host copies of O and LSE of
 every step are inside its timed region, pipelined over two device buffer sets
-(step i+1's uploads and step i-1's download overlap step i's kernel).  `roofline` relates the kernel to the measured dense
+(step i+1's uploads and step i-1's download overlap step i's kernel); beside it,
+the machine's host link rates, the bound they put on e2e, and the step's own copies
+timed alone (`step_copies_gbs`).  `roofline` relates the kernel to the measured dense
 bf16 tensor peak.  `cpu_baseline` times the fp64 oracle on a bounded sample of
 the same workload on the host cores.
 
@@ -467,6 +469,22 @@ def run_ours(args, w):
         host_out = {"dq": dq_h, "dk": dk_h, "dv": dv_h}
     sets = [bufs0, {name: torch.empty_like(t) for name, t in bufs0.items()}]
     up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    # the step's own copies, timed alone (outside the timed region): a box whose
+    # e2e falls far below link_bound shows here whether these buffers copy slower
+    step_copy = {}
+    for direction, pairs in (("h2d", [(sets[1][n], h) for n, h in host_in.items()]),
+                             ("d2h", [(h, sets[1][n]) for n, h in host_out.items()])):
+        best = 0.0
+        nbytes = sum(src.numel() * src.element_size() for _, src in pairs)
+        for _ in range(2):
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            with torch.cuda.stream(up):
+                for dst, src in pairs:
+                    dst.copy_(src, non_blocking=True)
+            torch.cuda.synchronize(dev)
+            best = max(best, nbytes / (time.perf_counter() - t0) / 1e9)
+        step_copy[direction] = best
     ev_up = [torch.cuda.Event() for _ in range(2)]
     ev_comp = [torch.cuda.Event() for _ in range(2)]
     ev_down = [torch.cuda.Event() for _ in range(2)]
@@ -553,6 +571,7 @@ def run_ours(args, w):
                 "pipelining": "two device buffer sets; uploads and downloads on their own streams "
                               "overlap the neighbouring steps' kernels",
                 "host_link_gbs": link,
+                "step_copies_gbs": step_copy,
                 "link_bound": link_bound(link, bytes_in, bytes_out, flops)},
         "gpu_launches": int(launches),
         "clocks": clk,
