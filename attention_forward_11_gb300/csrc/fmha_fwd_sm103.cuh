@@ -41,9 +41,10 @@
 // FMA and one ex2 (scale * log2e folded into the FMA), the running sum is
 // rescaled by alpha = 2^(m_old - m_new), and O is divided by the sum once at the
 // end.  The maximum used for the exponentials is only raised when a tile's
-// maximum exceeds it by more than 8 (log2 units); otherwise the stale maximum
-// is kept (weights stay <= 256; l and O share it, so the quotient is the same),
-// and O in tensor memory is rescaled only on the rare tiles that raise it.
+// maximum exceeds it by more than 15 (log2 units); otherwise the stale maximum
+// is kept (weights stay <= 2^15, inside the fp16 range of P; l and O share it, so
+// the quotient is the same), and O in tensor memory is rescaled only on the rare
+// tiles that raise it.
 // The weights of a tile are handed to the MMA warp in two halves of 64 keys, so
 // the first half of O += P.V runs while the second half's exponentials are made.
 // That hand-off uses hardware named barriers (softmax warps arrive, the MMA warp
@@ -97,7 +98,7 @@ static_assert(2 * kRegsSoftmax + kRegsEpilogue + kRegsOther <= 4 * (65536 / kThr
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 0;           // S_t at kTmemS + 128 t
 constexpr uint32_t kTmemO = 256;         // O_t at kTmemO + 128 t
-constexpr float kRescaleLog2 = 8.0f;     // raise the running max only past 2^8
+constexpr float kRescaleLog2 = 15.0f;    // raise the running max only past 2^15 (fp16 P holds 2^15)
 
 enum : int {
     BAR_QFULL = 0,
@@ -692,7 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          fmaxf(mx[6], mx[7]));
                 const float m_tile = tmax * sl2;
 
-                // raise the running max only when the tile max exceeds it by more than 2^8
+                // raise the running max only when the tile max exceeds it by more than 2^15
                 // (always on the first tile with a visible key: then alpha = 0)
                 float alpha = 1.f;
                 if (m_tile - m_run > kRescaleLog2) {
