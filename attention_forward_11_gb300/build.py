@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 SOURCES = [os.path.join(CSRC, "attn_api.cu")]
 HEADERS = [os.path.join(CSRC, f) for f in ("fmha_fwd_sm103.cuh", "fmha_fwd_d256_sm103.cuh", "fmha_bwd_sm103.cuh",
-                                          "unit_rates_sm103.cuh", "sm103_ptx.cuh")] + [
+                                          "fmha_bwd_d256_sm103.cuh", "unit_rates_sm103.cuh", "sm103_ptx.cuh")] + [
     os.path.join(ROOT, "include", "attn.h")]
 OUT = os.path.join(PKG, "libattn.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

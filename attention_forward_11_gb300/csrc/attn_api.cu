@@ -18,6 +18,7 @@
 
 #include "fmha_bwd_sm103.cuh"
 #include "fmha_fwd_d256_sm103.cuh"
+#include "fmha_bwd_d256_sm103.cuh"
 #include "fmha_fwd_sm103.cuh"
 #include "unit_rates_sm103.cuh"
 
@@ -79,6 +80,20 @@ bool opt_in_smem_bwd() {
                                 attn::bwd::DqGeo<kD>::kSmemBytes) == cudaSuccess;
 }
 
+template <int kRole, bool kF16>
+bool opt_in_smem_bwd256() {
+    return cudaFuncSetAttribute(attn::bwd256::fmha_bwd_d256_kernel<kRole, kF16>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                attn::bwd256::Geo<kRole>::kSmemBytes) == cudaSuccess;
+}
+
+template <bool kF16>
+bool opt_in_smem_bwd256_all() {
+    using namespace attn::bwd256;
+    return opt_in_smem_bwd256<kRoleDV, kF16>() && opt_in_smem_bwd256<kRoleDK, kF16>() &&
+           opt_in_smem_bwd256<kRoleDQ, kF16>();
+}
+
 // Per-device one-time set-up: the kernels' shared-memory opt-in and the SM count.
 bool device_setup(int dev, int* sm_count) {
     static std::mutex mu;
@@ -92,7 +107,7 @@ bool device_setup(int dev, int* sm_count) {
             !opt_in_smem<attn::PlainSched, true, 64>() || !opt_in_smem<attn::SplitSched, false, 64>() ||
             !opt_in_smem<attn::TableSched, false, 128>() || !opt_in_smem<attn::TableSched, true, 128>() ||
             !opt_in_smem_bwd<false, 128>() || !opt_in_smem_bwd<true, 128>() || !opt_in_smem_bwd<false, 64>() ||
-            !opt_in_smem_bwd<true, 64>() ||
+            !opt_in_smem_bwd<true, 64>() || !opt_in_smem_bwd256_all<false>() || !opt_in_smem_bwd256_all<true>() ||
             cudaFuncSetAttribute(attn::d256::fmha_fwd_d256_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  attn::d256::Geo::kSmemBytes) != cudaSuccess ||
             cudaFuncSetAttribute(attn::d256::fmha_fwd_d256_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -614,6 +629,36 @@ attn_status_t launch_bwd(const CUtensorMap* tm, const void* o, const void* dO, c
     return ATTN_OK;
 }
 
+// Head size 256: the prep kernel, then the dV, dK and dQ launches of the one
+// D = 256 kernel (each persistent, on its own work counter).
+template <bool kF16>
+attn_status_t launch_bwd256(const CUtensorMap* tm, const void* o, const void* dO, const float* lse,
+                            const attn::bwd::BwdParams& p, int sms, cudaStream_t stream) {
+    using namespace attn::bwd256;
+    constexpr int kD = 256;
+    const long long rows = (long long)p.Hq * p.sq_pad;  // per batch entry
+    const long long per_block = 8LL * attn::bwd::prep_rows_per_warp<kD>();
+    const dim3 prep_grid(static_cast<unsigned int>((rows + per_block - 1) / per_block), static_cast<unsigned int>(p.B));
+    attn::bwd::bwd_prep_kernel<kF16, kD><<<prep_grid, 256, 0, stream>>>(
+        static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dO), lse, p);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    auto grid_of = [&](int n) { return static_cast<unsigned int>(n < sms ? n : sms); };
+    fmha_bwd_d256_kernel<kRoleDV, kF16><<<grid_of(n_items_of<kRoleDV>(p)), kThreads, Geo<kRoleDV>::kSmemBytes,
+                                          stream>>>(tm[0], tm[1], tm[2], tm[3], p);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    fmha_bwd_d256_kernel<kRoleDK, kF16><<<grid_of(n_items_of<kRoleDK>(p)), kThreads, Geo<kRoleDK>::kSmemBytes,
+                                          stream>>>(tm[0], tm[1], tm[2], tm[3], p);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    fmha_bwd_d256_kernel<kRoleDQ, kF16><<<grid_of(n_items_of<kRoleDQ>(p)), kThreads, Geo<kRoleDQ>::kSmemBytes,
+                                          stream>>>(tm[0], tm[1], tm[2], tm[3], p);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return ATTN_OK;
+}
+
 }  // namespace
 
 extern "C" attn_status_t attn_bwd_workspace_size(int B, int Sq, int Skv, int Hq, int Hkv, int D, size_t* bytes) {
@@ -621,8 +666,7 @@ extern "C" attn_status_t attn_bwd_workspace_size(int B, int Sq, int Skv, int Hq,
     *bytes = 0;
     const attn_status_t st = check_sizes(B, Sq, Skv, Hq, Hkv, D, 0);
     if (st != ATTN_OK) return st;
-    if (D == 256) return ATTN_ERR_UNSUPPORTED;  // the backward kernels take D <= 128
-    *bytes = 2 * bwd_vec_bytes(B, Sq, Hq) + kBwdAlign;  // + the dK/dV kernel's work counter
+    *bytes = 2 * bwd_vec_bytes(B, Sq, Hq) + kBwdAlign;  // + the kernels' work counters
     return ATTN_OK;
 }
 
@@ -634,7 +678,6 @@ extern "C" attn_status_t attn_bwd(const void* q, const void* k, const void* v, c
     if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !workspace) return ATTN_ERR_INVALID_ARG;
     if (dtype != ATTN_DTYPE_BF16 && dtype != ATTN_DTYPE_F16) return ATTN_ERR_INVALID_ARG;
     attn_status_t st = check_sizes(B, Sq, Skv, Hq, Hkv, D, causal);
-    if (st == ATTN_OK && D == 256) st = ATTN_ERR_UNSUPPORTED;  // the backward kernels take D <= 128
     if (st == ATTN_ERR_INVALID_ARG) return st;
     if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
     for (const void* ptr : {q, k, v, o, dO, static_cast<const void*>(dq), static_cast<const void*>(dk),
@@ -690,6 +733,9 @@ extern "C" attn_status_t attn_bwd(const void* q, const void* k, const void* v, c
         return ATTN_ERR_CUDA;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || !device_setup(dev, &sms)) return ATTN_ERR_CUDA;
+    if (D == 256)
+        return f16 ? launch_bwd256<true>(tm, o, dO, lse, p, sms, stream)
+                   : launch_bwd256<false>(tm, o, dO, lse, p, sms, stream);
     if (D == 64)
         return f16 ? launch_bwd<true, 64>(tm, o, dO, lse, p, sms, stream)
                    : launch_bwd<false, 64>(tm, o, dO, lse, p, sms, stream);

@@ -137,7 +137,7 @@ struct BwdParams {
     uint16_t* dq;               // [B, Sq, Hq, D]
     uint16_t* dk;               // [B, Skv, Hkv, D]
     uint16_t* dv;               // [B, Skv, Hkv, D]
-    int* work;                  // work-item counters of the dK/dV ([0]) and dQ ([1]) kernels (zeroed by prep)
+    int* work;                  // work-item counters (zeroed by prep): dK/dV or dV ([0]), dQ ([1]), dK ([2])
     int n_q_tiles, n_kv_tiles;
     unsigned int poll_limit;
 };
@@ -225,7 +225,8 @@ __global__ void __launch_bounds__(256)
     constexpr int kR = 32 / kL;         // rows per load instruction
     const int lane = static_cast<int>(threadIdx.x) & 31;
     const int b = static_cast<int>(blockIdx.y);
-    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) p.work[0] = p.work[1] = 0;  // the two queues
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)  // the work queues
+        p.work[0] = p.work[1] = p.work[2] = 0;
     const int per_batch = p.sq_pad * p.Hq;  // rows (i, h) of one batch entry, in memory order
     const int row0 = (static_cast<int>(blockIdx.x) * 8 + static_cast<int>(threadIdx.x) / 32) * (kR * kPrepIters);
     uint4 ov[kPrepIters], dv[kPrepIters];

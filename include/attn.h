@@ -165,7 +165,7 @@ attn_status_t attn_fwd_splitkv_noalloc(const void* q, const void* k, const void*
  *           keys no query row sees)
  * B .. scale  as attn_fwd (the same causal mode and scale as the forward call;
  *           the page's backward has no mask, this one applies the forward's);
- *           D 64 or 128 (D = 256: ATTN_ERR_UNSUPPORTED); B <= 65535.
+ *           D 64, 128 or 256; B <= 65535.
  * dtype     ATTN_DTYPE_BF16 or ATTN_DTYPE_F16: the element type of q, k, v, o,
  *           dO, dq, dk and dv.
  * workspace device pointer, 256-byte aligned, of at least
@@ -177,8 +177,9 @@ attn_status_t attn_fwd_splitkv_noalloc(const void* q, const void* k, const void*
  * Ownership: the caller owns every buffer.  q, k, v, o, dO, dq, dk, dv must be
  * 16-byte aligned; lse 4-byte aligned.  dq, dk, dv and the workspace must not
  * overlap any input or each other.  Three kernels are enqueued on `stream`
- * (prep, dK/dV, dQ); errors are reported as for attn_fwd (nothing is launched
- * on any error return; a device-side timeout shows in attn_last_device_status).
+ * (prep, dK/dV, dQ), four at D = 256 (prep, dV, dK, dQ); errors are reported
+ * as for attn_fwd (nothing is launched on any error return; a device-side
+ * timeout shows in attn_last_device_status).
  */
 attn_status_t attn_bwd_workspace_size(int B, int Sq, int Skv, int Hq, int Hkv, int D, size_t* bytes);
 attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,

@@ -146,6 +146,12 @@ CASES = [
     (1, 1000, 1000, 2, 1, 128, 0),
     (1, 384, 384, 2, 2, 64, 1),       # head size 64
     (1, 250, 390, 4, 2, 64, 2),
+    (1, 256, 256, 2, 2, 256, 0),      # head size 256: the dV, dK and dQ launches
+    (1, 300, 300, 4, 2, 256, 1),
+    (2, 200, 333, 4, 1, 256, 1),
+    (1, 333, 200, 2, 1, 256, 1),
+    (1, 200, 333, 2, 2, 256, 2),
+    (1, 1000, 700, 2, 2, 256, 0),
 ]
 
 
@@ -158,7 +164,8 @@ def test_bwd_matches_oracle(case):
 
 
 @pytest.mark.parametrize("case", [(1, 256, 256, 2, 2, 128, 1), (2, 200, 333, 4, 1, 128, 1),
-                                  (1, 1000, 1000, 2, 1, 128, 0), (1, 384, 384, 2, 2, 64, 1)],
+                                  (1, 1000, 1000, 2, 1, 128, 0), (1, 384, 384, 2, 2, 64, 1),
+                                  (1, 384, 384, 2, 2, 256, 1)],
                          ids=lambda c: "B{}_Sq{}_Skv{}_H{}-{}_D{}_c{}".format(*c))
 def test_bwd_after_gpu_forward(case):
     """O and LSE from attn_fwd, as a training step runs them, against the exact
@@ -170,7 +177,8 @@ def test_bwd_after_gpu_forward(case):
     check(q, k, v, do, causal, 1 / math.sqrt(shape[5]), str(case), fwd="gpu")
 
 
-@pytest.mark.parametrize("case", [(1, 300, 300, 2, 1, 128, 1), (1, 200, 260, 2, 2, 64, 0)])
+@pytest.mark.parametrize("case", [(1, 300, 300, 2, 1, 128, 1), (1, 200, 260, 2, 2, 64, 0),
+                                  (1, 250, 300, 2, 1, 256, 1)])
 def test_bwd_f16_matches_oracle(case):
     *shape, causal = case
     q, k, v, do = problem(*shape, seed=sum(case), dtype="f16")
@@ -178,12 +186,13 @@ def test_bwd_f16_matches_oracle(case):
     check(q, k, v, do, causal, scale, str(case), dtype="f16")
 
 
+@pytest.mark.parametrize("D", [128, 256])
 @pytest.mark.parametrize("causal", [0, 1, 2])
 @pytest.mark.parametrize("Sq,Skv", [(1, 300), (300, 1), (1, 1), (7, 5)])
-def test_bwd_degenerate_lengths(Sq, Skv, causal):
-    q, k, v, do = problem(2, Sq, Skv, 4, 2, 128, seed=Sq + 3 * Skv + causal)
+def test_bwd_degenerate_lengths(Sq, Skv, causal, D):
+    q, k, v, do = problem(2, Sq, Skv, 4, 2, D, seed=Sq + 3 * Skv + causal + D)
     scale = 0.125
-    check(q, k, v, do, causal, scale, f"Sq={Sq} Skv={Skv} causal={causal}")
+    check(q, k, v, do, causal, scale, f"Sq={Sq} Skv={Skv} causal={causal} D={D}")
 
 
 def test_bwd_many_tiny_batch_entries():
@@ -192,30 +201,33 @@ def test_bwd_many_tiny_batch_entries():
         check(q, k, v, do, causal, 0.1, f"B=64 causal={causal}")
 
 
-def test_bwd_exact_zeros():
+@pytest.mark.parametrize("D", [128, 256])
+def test_bwd_exact_zeros(D):
     """Keys that no row sees (top-left mask, Skv > Sq) get dk = dv = 0 exactly;
     rows that see no key (bottom-right mask, Sq > Skv) get dq = 0 exactly."""
-    q, k, v, do = problem(1, 130, 400, 2, 1, 128, seed=82)
+    q, k, v, do = problem(1, 130, 400, 2, 1, D, seed=82)
     dq, dk, dv = gpu_grads(q, k, v, do, 2, 0.1)
     assert np.all(dk[:, 130:] == 0.0) and np.all(dv[:, 130:] == 0.0)
     assert np.abs(dk[:, :130]).max() > 0 and np.abs(dv[:, :130]).max() > 0
-    q, k, v, do = problem(1, 400, 130, 2, 1, 128, seed=83)
+    q, k, v, do = problem(1, 400, 130, 2, 1, D, seed=83)
     dq, dk, dv = gpu_grads(q, k, v, do, 1, 0.1)
     assert np.all(dq[:, : 400 - 130] == 0.0)
     assert np.abs(dq[:, 400 - 130:]).max() > 0
 
 
-def test_bwd_zero_output_gradient():
-    q, k, v, do = problem(1, 300, 300, 2, 2, 128, seed=84)
+@pytest.mark.parametrize("D", [128, 256])
+def test_bwd_zero_output_gradient(D):
+    q, k, v, do = problem(1, 300, 300, 2, 2, D, seed=84)
     do = np.zeros_like(do)
     for g in gpu_grads(q, k, v, do, 1, 0.1):
         assert np.all(g == 0.0)
 
 
-def test_bwd_is_deterministic():
+@pytest.mark.parametrize("D", [128, 256])
+def test_bwd_is_deterministic(D):
     """No atomics: two calls give bit-identical gradients."""
     import torch
-    q, k, v, do = problem(2, 700, 700, 4, 2, 128, seed=85)
+    q, k, v, do = problem(2, 700, 700, 4, 2, D, seed=85)
     a = gpu_grads(q, k, v, do, 1, 0.1, raw=True)
     b = gpu_grads(q, k, v, do, 1, 0.1, raw=True)
     for x, y in zip(a, b):
@@ -265,17 +277,19 @@ def test_bwd_gqa_sampled():
     _sampled((1, 2048, 2048, 8, 2, 128), 1, seed=87, n_rows=32, kv_pairs=[(0, 1)])
 
 
-@pytest.mark.parametrize("Sq,Skv,causal", [(128, 8192, 2), (8192, 128, 1), (200, 6000, 2)],
-                         ids=["keys_unseen", "rows_unseeing", "ragged_unseen"])
-def test_bwd_queues_with_mostly_empty_items(Sq, Skv, causal):
+@pytest.mark.parametrize("Sq,Skv,causal,D", [(128, 8192, 2, 128), (8192, 128, 1, 128), (200, 6000, 2, 128),
+                                             (128, 4096, 2, 256), (4096, 128, 1, 256)],
+                         ids=["keys_unseen", "rows_unseeing", "ragged_unseen", "keys_unseen_d256",
+                              "rows_unseeing_d256"])
+def test_bwd_queues_with_mostly_empty_items(Sq, Skv, causal, D):
     """More work items than SMs, nearly all of them empty: with a top-left mask
     and Skv >> Sq most KV tiles are seen by no row (the dK/dV queue), with a
     bottom-right mask and Sq >> Skv most query tiles see no key (the dQ queue).
     Empty items write exact zeros and must not upset the barrier phases of the
     items around them."""
-    q, k, v, do = problem(1, Sq, Skv, 8, 8, 128, seed=Sq + Skv + causal)
-    check(q, k, v, do, causal, 1 / math.sqrt(128), f"Sq={Sq} Skv={Skv} causal={causal}")
-    dq, dk, dv = gpu_grads(q, k, v, do, causal, 1 / math.sqrt(128))
+    q, k, v, do = problem(1, Sq, Skv, 8, 8, D, seed=Sq + Skv + causal)
+    check(q, k, v, do, causal, 1 / math.sqrt(D), f"Sq={Sq} Skv={Skv} causal={causal} D={D}")
+    dq, dk, dv = gpu_grads(q, k, v, do, causal, 1 / math.sqrt(D))
     if causal == 2:
         assert np.all(dk[:, Sq:] == 0.0) and np.all(dv[:, Sq:] == 0.0)
     else:
@@ -304,3 +318,19 @@ def test_bwd_long_noncausal_shape_sampled():
     got_dv = np.array([dv[b, j, g] for b, g, j in keys])
     compare((got_dq, got_dk, got_dv), (ref_dq, ref_dk, ref_dv), "bf16", "long non-causal sampled",
             term_sizes(q, k, v, do, scale))
+
+
+def test_bwd_d256_shape_sampled():
+    """B=4, H=16, S=4096, D=256, causal (the forward's head-size-256 benchmark
+    shape): sampled dq rows and dk/dv keys of two (batch, head) pairs."""
+    _sampled((4, 4096, 4096, 16, 16, 256), 1, seed=91, n_rows=32, kv_pairs=[(0, 3), (3, 12)])
+
+
+def test_bwd_d256_every_element():
+    """Head size 256 with every element of dq, dk and dv against the oracle:
+    GQA group 2, 2048 rows and keys (16 tiles each way), causal."""
+    B, S, Hq, Hkv, D = 1, 2048, 4, 2, 256
+    q, k, v, do = problem(B, S, S, Hq, Hkv, D, seed=92)
+    stats = check(q, k, v, do, 1, 1 / math.sqrt(D), "d256 every element")
+    print("d256 every element, (mean, max excess) in u rms:",
+          {k_: (round(a, 3), round(b, 2)) for k_, (a, b) in stats.items()})

@@ -193,23 +193,24 @@ def test_bwd_invalid_arguments_rejected(lib, over):
     assert call_bwd(**over) == fa.ATTN_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("D", [32, 96, 256])
+@pytest.mark.parametrize("D", [32, 96, 192])
 def test_bwd_other_head_dims_unsupported(lib, D):
     assert call_bwd(D=D) == fa.ATTN_ERR_UNSUPPORTED
 
 
 def test_bwd_workspace_size(lib):
     # two fp32 vectors of B * Hq * (Sq rounded up to 128) entries, each rounded up to 256
-    # bytes, and 256 bytes for the dK/dV kernel's work counter
+    # bytes, and 256 bytes for the kernels' work counters; the same at every head size
     assert fa.attn_bwd_workspace_size(1, 256, 256, 2, 2, 128) == 2 * 2 * 256 * 4 + 256
+    assert fa.attn_bwd_workspace_size(1, 256, 256, 2, 2, 256) == 2 * 2 * 256 * 4 + 256
     assert fa.attn_bwd_workspace_size(3, 129, 7, 5, 1, 64) == 2 * 3 * 5 * 256 * 4 + 256
     assert fa.attn_bwd_workspace_size(1, 1, 1, 1, 1, 128) == 2 * 512 + 256
     assert lib.attn_bwd_workspace_size(1, 256, 256, 2, 2, 128, None) == fa.ATTN_ERR_INVALID_ARG
     with pytest.raises(fa.AttnError) as e:
         fa.attn_bwd_workspace_size(1, 256, 256, 3, 2, 128)
     assert e.value.status == fa.ATTN_ERR_INVALID_ARG
-    with pytest.raises(fa.AttnError) as e:  # the forward takes D = 256, the backward does not
-        fa.attn_bwd_workspace_size(1, 256, 256, 2, 2, 256)
+    with pytest.raises(fa.AttnError) as e:
+        fa.attn_bwd_workspace_size(1, 256, 256, 2, 2, 192)
     assert e.value.status == fa.ATTN_ERR_UNSUPPORTED
 
 
