@@ -35,10 +35,12 @@
 // S buffer, each group of elementwise warps over the start of its own columns,
 // as in the D <= 128 kernels.
 //
-// Warps as in the D <= 128 backward (320 threads): eight elementwise warps (TMEM
-// lane quarter x column half), the MMA warp, the TMA warp (then the release warp
-// of the abort path).  The elementwise warps hand over to the MMA warp through
-// hardware named barriers; every mbarrier wait is bounded.
+// Warps (352 threads): eight elementwise warps (TMEM lane quarter x column half),
+// the MMA warp, the TMA warp (then the release warp of the abort path) and a ring
+// watcher.  The elementwise warps and the watcher hand over to the MMA warp through
+// hardware named barriers, so within an item the MMA warp polls no mbarrier (such
+// a poll would first wait for its queued MMAs to drain), and each half's products
+// start as soon as that half has landed.  Every mbarrier wait is bounded.
 #pragma once
 #include <cstdint>
 #include <cuda.h>
@@ -54,7 +56,8 @@ using bwd::kCols;
 using bwd::kComputeWarps;
 using bwd::kLoadWarp;
 using bwd::kMmaWarp;
-using bwd::kThreads;
+constexpr int kWatchWarp = kLoadWarp + 1;
+constexpr int kThreads = 32 * (kWatchWarp + 1);  // 352
 
 enum Role : int { kRoleDV = 0, kRoleDK = 1, kRoleDQ = 2 };
 
@@ -70,6 +73,13 @@ constexpr int kMaxSlots = 5;
 // synced for P_n (S_{n+1} is issued before that sync), so consecutive steps must
 // not share a barrier; step n+2 needs S_{n+2}, issued only after the sync for n.
 constexpr uint32_t kBarSRead = 2, kBarDsReady = 3, kBarP0 = 2;
+// Ring hand-off: the watcher warp polls each slot's "landed" mbarrier and arrives
+// on that slot's named barrier (kBarRing0 + slot), where the MMA warp syncs before
+// the half's MMAs: an mbarrier poll by the MMA warp itself would first wait for its
+// queued MMAs to drain.  Fill f + kSlots reuses slot f's barrier only after the MMA
+// warp consumed fill f (its commit frees the slot for the refill), so generations
+// never mix.
+constexpr uint32_t kBarRing0 = 4, kBarRingThreads = 64;
 
 enum : int {
     B_A1FULL = 0,                  // the item's first resident tile landed
@@ -100,7 +110,9 @@ struct Geo {
     static constexpr int kAbort = kTmemSlot + 4;
     static constexpr int kItems = kAbort + 4;    // [2] published work items
     static constexpr int kMmaExit = kItems + 8;  // set once the MMA warp left its loop
-    static constexpr int kSmemBytes = kMmaExit + 4 + 1024;
+    static constexpr int kFills = kMmaExit + 4;  // ring fills the producer issued in all
+    static constexpr int kProdDone = kFills + 4; // set once kFills is final
+    static constexpr int kSmemBytes = kProdDone + 4 + 1024;
     static_assert(kSlots <= kMaxSlots, "barrier area");
     static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
     static constexpr uint32_t kTmemS = 0, kTmemDP = 128, kTmemAcc = 256;
@@ -207,6 +219,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + G::kAbort);
     volatile int* item_slot = reinterpret_cast<volatile int*>(smem + G::kItems);
     volatile int* mma_exit = reinterpret_cast<volatile int*>(smem + G::kMmaExit);
+    volatile int* fills_total = reinterpret_cast<volatile int*>(smem + G::kFills);
+    volatile int* prod_done = reinterpret_cast<volatile int*>(smem + G::kProdDone);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::kTmemSlot);
     auto bar = [&](int i) -> uint32_t { return sbase + G::kBar + 8 * i; };
     const int n_items = n_items_of<kRole>(p);
@@ -234,6 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(B_MMADONE), 1);
         *abort_flag = 0;
         *mma_exit = 0;
+        *fills_total = 0;
+        *prod_done = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_do);
@@ -320,6 +336,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!ok) break;
             }
+            *fills_total = f;  // the watcher stops after this many fills
+            __threadfence_block();
+            *prod_done = 1;
             // drain: every copy issued has landed before the CTA may exit
             if (a1 > 0) drain_bounded(bar(B_A1FULL), (a1 - 1) & 1, limit);
             if (a2 > 0) drain_bounded(bar(B_A2FULL), (a2 - 1) & 1, limit);
@@ -329,8 +348,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
-        // release warp of the abort path: the elementwise warps' arrivals
-        bwd::release_named_barriers(mma_exit, abort_flag, 2, 2, kBarReadyThreads, kComputeWarps, limit);
+        // release warp of the abort path: the elementwise warps' and the watcher's
+        // arrivals (see bwd::release_named_barriers)
+        const unsigned long long cap = 64ull * limit;
+        unsigned long long i = 0;
+        for (; i < cap && !*mma_exit; ++i) {
+            if (*abort_flag) {
+                for (int id = 0; id < 2; ++id)
+                    for (int k = 0; k < kComputeWarps; ++k) named_bar_arrive(2 + id, kBarReadyThreads);
+                for (int s = 0; s < G::kSlots; ++s) named_bar_arrive(kBarRing0 + s, kBarRingThreads);
+            } else {
+                nanosleep_ns(1024);
+            }
+        }
+        if (i == cap) atomicOr(&g_attn_status, kStatusTimeout);
+    } else if (warp == kWatchWarp) {
+        // =========================== ring watcher ===========================
+        // Fill f landed -> arrive on its slot's named barrier.  Stops once the
+        // producer has finished and every fill it issued was handed over.
+        for (int f = 0;; ++f) {
+            const int s = f % G::kSlots;
+            bool landed = false;
+            unsigned int i = 0;
+            for (; i < limit; ++i) {
+                if (mbar_try_wait(bar(B_FULL + s), (f / G::kSlots) & 1)) {
+                    landed = true;
+                    break;
+                }
+                if ((i & 15u) == 15u && (*abort_flag || (*prod_done && f >= *fills_total))) break;
+            }
+            if (!__all_sync(0xffffffffu, landed)) {
+                if (i == limit) {
+                    *abort_flag = 1;
+                    atomicOr(&g_attn_status, kStatusTimeout);
+                }
+                break;
+            }
+            named_bar_arrive(kBarRing0 + s, kBarRingThreads);
+        }
     } else if (warp == kMmaWarp) {
         // =========================== MMA issuer =============================
         constexpr uint32_t idesc_s = idesc_f16kind_f32(kBM, kBN, false, kF16);  // S, dP (or transposed)
@@ -343,13 +398,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         int f = 0, g = 0, w = 0;  // ring fills consumed, steps (over all items), items with work
         int s_issued = 0;         // S products issued (3-product roles: the S read-out sync count)
-        // both halves of the next product's streamed operand have landed
-        auto wait_pair = [&]() -> bool {
-            for (int hh = 0; hh < 2; ++hh)
-                if (!wait_bounded(bar(B_FULL + (f + hh) % G::kSlots), ((f + hh) / G::kSlots) & 1, abort_flag, limit))
-                    return false;
+        // fill ff landed (the watcher's hand-off); then its MMAs may be issued
+        auto half_ready = [&](int ff) {
+            named_bar_sync(kBarRing0 + static_cast<uint32_t>(ff % G::kSlots), kBarRingThreads);
             tc_fence_after();
-            return true;
         };
         for (int j = 0; ok; ++j) {
             const int slot = j & 1;
@@ -374,20 +426,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    if (!wait_pair()) {
-                        ok = false;
-                        break;
-                    }
                     const uint32_t d = tmem_base + (kThree ? G::kTmemS : 128u * static_cast<uint32_t>(gs & 1));
-                    if (elect_one()) {
-                        for (int hh = 0; hh < 2; ++hh) {
+                    for (int hh = 0; hh < 2; ++hh) {
+                        half_ready(f + hh);
+                        if (elect_one()) {
                             mma_s_half(d, a1_desc, ring_k, (f + hh) % G::kSlots, hh, idesc_s);
                             mma_commit(bar(B_EMPTY + (f + hh) % G::kSlots));
+                            if (hh == 1) {
+                                mma_commit(bar(B_SFULL + (kThree ? 0 : (gs & 1))));
+                                if (step == N - 1) mma_commit(bar(B_A1EMPTY));  // the item's last S
+                            }
                         }
-                        mma_commit(bar(B_SFULL + (kThree ? 0 : (gs & 1))));
-                        if (step == N - 1) mma_commit(bar(B_A1EMPTY));  // the item's last S
+                        __syncwarp();
                     }
-                    __syncwarp();
                     ++s_issued;
                 } else if (kind == kX2) {
                     // dP_step = A2 X2^T (3-product roles only)
@@ -395,40 +446,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    if (!wait_pair()) {
-                        ok = false;
-                        break;
-                    }
-                    if (elect_one()) {
-                        for (int hh = 0; hh < 2; ++hh) {
+                    for (int hh = 0; hh < 2; ++hh) {
+                        half_ready(f + hh);
+                        if (elect_one()) {
                             mma_s_half(tmem_base + G::kTmemDP, a2_desc, ring_k, (f + hh) % G::kSlots, hh, idesc_s);
                             mma_commit(bar(B_EMPTY + (f + hh) % G::kSlots));
+                            if (hh == 1) {
+                                mma_commit(bar(B_DPFULL));
+                                if (step == N - 1) mma_commit(bar(B_A2EMPTY));  // the item's last dP
+                            }
                         }
-                        mma_commit(bar(B_DPFULL));
-                        if (step == N - 1) mma_commit(bar(B_A2EMPTY));  // the item's last dP
+                        __syncwarp();
                     }
-                    __syncwarp();
                 } else {
                     // acc[:, 128 h .. +128) (+)= E_step Y_h, E = dS (over dP) or P (over its S buffer)
                     if constexpr (kThree)
                         named_bar_sync(kBarDsReady, kBarReadyThreads);
                     else
                         named_bar_sync(kBarP0 + static_cast<uint32_t>(gs & 1), kBarReadyThreads);
-                    if (!wait_pair()) {
-                        ok = false;
-                        break;
-                    }
+                    tc_fence_after();
                     const uint32_t tE = tmem_base + (kThree ? G::kTmemDP : 128u * static_cast<uint32_t>(gs & 1));
-                    if (elect_one()) {
-                        for (int hh = 0; hh < 2; ++hh) {
+                    for (int hh = 0; hh < 2; ++hh) {
+                        half_ready(f + hh);
+                        if (elect_one()) {
                             bwd::mma_tmem_mn(tAcc + 128 * hh, tE,
                                              ring_mn + static_cast<uint64_t>((((f + hh) % G::kSlots) * kHalf) >> 4),
                                              idesc_acc, step > 0);
                             mma_commit(bar(B_EMPTY + (f + hh) % G::kSlots));
+                            if (hh == 1 && step == N - 1) mma_commit(bar(B_ACCDONE));
                         }
-                        if (step == N - 1) mma_commit(bar(B_ACCDONE));
+                        __syncwarp();
                     }
-                    __syncwarp();
                 }
                 f += 2;
             }
