@@ -100,6 +100,7 @@ enum : int {
 template <int kRole>
 struct Geo {
     static constexpr bool kThree = kRole != kRoleDV;   // S, dP and the accumulator
+    static constexpr bool kWatch = kThree;             // ring hand-off through the watcher warp
     static constexpr int kResident = kThree ? 2 : 1;   // resident 64 KB tiles
     static constexpr int kSlots = kThree ? 3 : 5;      // ring slots of 32 KB
     static constexpr int kRes0 = 0;
@@ -356,7 +357,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (*abort_flag) {
                 for (int id = 0; id < 2; ++id)
                     for (int k = 0; k < kComputeWarps; ++k) named_bar_arrive(2 + id, kBarReadyThreads);
-                for (int s = 0; s < G::kSlots; ++s) named_bar_arrive(kBarRing0 + s, kBarRingThreads);
+                if constexpr (G::kWatch)
+                    for (int s = 0; s < G::kSlots; ++s) named_bar_arrive(kBarRing0 + s, kBarRingThreads);
             } else {
                 nanosleep_ns(1024);
             }
@@ -366,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // =========================== ring watcher ===========================
         // Fill f landed -> arrive on its slot's named barrier.  Stops once the
         // producer has finished and every fill it issued was handed over.
-        for (int f = 0;; ++f) {
+        for (int f = 0; G::kWatch; ++f) {
             const int s = f % G::kSlots;
             bool landed = false;
             unsigned int i = 0;
@@ -398,10 +400,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         int f = 0, g = 0, w = 0;  // ring fills consumed, steps (over all items), items with work
         int s_issued = 0;         // S products issued (3-product roles: the S read-out sync count)
-        // fill ff landed (the watcher's hand-off); then its MMAs may be issued
-        auto half_ready = [&](int ff) {
-            named_bar_sync(kBarRing0 + static_cast<uint32_t>(ff % G::kSlots), kBarRingThreads);
+        // Half hh of the product whose first fill is f has landed.  With the watcher:
+        // its hand-off, per half.  Without (dV, whose deeper ring is usually full
+        // ahead): one poll of both halves' barriers before the first half, measured
+        // faster there than the watcher.
+        auto half_ready = [&](int hh) -> bool {
+            if constexpr (G::kWatch) {
+                named_bar_sync(kBarRing0 + static_cast<uint32_t>((f + hh) % G::kSlots), kBarRingThreads);
+            } else {
+                if (hh == 0)
+                    for (int k = 0; k < 2; ++k)
+                        if (!wait_bounded(bar(B_FULL + (f + k) % G::kSlots), ((f + k) / G::kSlots) & 1, abort_flag,
+                                          limit))
+                            return false;
+            }
             tc_fence_after();
+            return true;
         };
         for (int j = 0; ok; ++j) {
             const int slot = j & 1;
@@ -428,7 +442,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const uint32_t d = tmem_base + (kThree ? G::kTmemS : 128u * static_cast<uint32_t>(gs & 1));
                     for (int hh = 0; hh < 2; ++hh) {
-                        half_ready(f + hh);
+                        if (!half_ready(hh)) {
+                            ok = false;
+                            break;
+                        }
                         if (elect_one()) {
                             mma_s_half(d, a1_desc, ring_k, (f + hh) % G::kSlots, hh, idesc_s);
                             mma_commit(bar(B_EMPTY + (f + hh) % G::kSlots));
@@ -447,7 +464,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     for (int hh = 0; hh < 2; ++hh) {
-                        half_ready(f + hh);
+                        if (!half_ready(hh)) {
+                            ok = false;
+                            break;
+                        }
                         if (elect_one()) {
                             mma_s_half(tmem_base + G::kTmemDP, a2_desc, ring_k, (f + hh) % G::kSlots, hh, idesc_s);
                             mma_commit(bar(B_EMPTY + (f + hh) % G::kSlots));
@@ -467,7 +487,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     const uint32_t tE = tmem_base + (kThree ? G::kTmemDP : 128u * static_cast<uint32_t>(gs & 1));
                     for (int hh = 0; hh < 2; ++hh) {
-                        half_ready(f + hh);
+                        if (!half_ready(hh)) {
+                            ok = false;
+                            break;
+                        }
                         if (elect_one()) {
                             bwd::mma_tmem_mn(tAcc + 128 * hh, tE,
                                              ring_mn + static_cast<uint64_t>((((f + hh) % G::kSlots) * kHalf) >> 4),
@@ -478,6 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         __syncwarp();
                     }
                 }
+                if (!ok) break;
                 f += 2;
             }
             if (!ok) break;
@@ -598,6 +622,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_before();
                     named_bar_arrive(kBarP0 + static_cast<uint32_t>(gs & 1), kBarReadyThreads);
                 } else {
+                    // dK: this group's delta, 32 columns at a time, each loaded one piece
+                    // ahead (the first before the wait) so its latency is hidden
+                    float dv[32];
+                    auto load_delta = [&](int c0) {
+#pragma unroll
+                        for (int c = 0; c < 32; c += 4) {
+                            if constexpr (kRole == kRoleDK) {
+                                const float4 d4 = *reinterpret_cast<const float4*>(dlv + c0 + c);
+                                dv[c] = d4.x;
+                                dv[c + 1] = d4.y;
+                                dv[c + 2] = d4.z;
+                                dv[c + 3] = d4.w;
+                            } else {
+                                dv[c] = dv[c + 1] = dv[c + 2] = dv[c + 3] = dlt;
+                            }
+                        }
+                    };
+                    load_delta(0);
                     const bool got2 = wait_bounded(bar(B_DPFULL), gs & 1, abort_flag, limit);
                     if (!__all_sync(0xffffffffu, got2)) {
                         ok = false;
@@ -611,20 +653,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         uint32_t y[32];
                         tmem_ld32(tDP + hc, y);
                         tmem_wait_ld_regs(y);
-                        float dv[32];
-                        if constexpr (kRole == kRoleDQ) {
-#pragma unroll
-                            for (int c = 0; c < 32; ++c) dv[c] = dlt;
-                        } else {
-#pragma unroll
-                            for (int c = 0; c < 32; c += 4) {
-                                const float4 d4 = *reinterpret_cast<const float4*>(dlv + hc + c);
-                                dv[c] = d4.x;
-                                dv[c + 1] = d4.y;
-                                dv[c + 2] = d4.z;
-                                dv[c + 3] = d4.w;
-                            }
-                        }
                         uint32_t pk[16];
 #pragma unroll
                         for (int c = 0; c < 32; c += 2) {
@@ -633,6 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                           __uint_as_float(y[c + 1]), dv[c], dv[c + 1]);
                             pk[c / 2] = pack_x2<kF16>(d0, d1);
                         }
+                        if (hc + 32 < kCols) load_delta(hc + 32);
                         tmem_st16(tDP + hc / 2, pk);
                     }
                     tmem_wait_st();
