@@ -327,11 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     for (int hh = 0; hh < 2; ++hh, ++f) {
                         const int s = f % G::kSlots, use = f / G::kSlots;
-                        // the slot is free and its previous fill has landed: a barrier is
-                        // re-armed only once the earlier fill's bytes are all counted, even
-                        // if an abort released the MMA warp before that fill landed
-                        if (use > 0 && !(wait_bounded(bar(B_EMPTY + s), (use - 1) & 1, abort_flag, limit) &&
-                                         wait_bounded(bar(B_FULL + s), (use - 1) & 1, abort_flag, limit))) {
+                        if (use > 0 && !wait_bounded(bar(B_EMPTY + s), (use - 1) & 1, abort_flag, limit)) {
                             ok = false;
                             break;
                         }
@@ -354,7 +350,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         // release warp of the abort path: the elementwise warps' and the watcher's
-        // arrivals (see bwd::release_named_barriers)
+        // arrivals (see bwd::release_named_barriers).  It starts only after the loop
+        // above has stopped re-arming slots and drained every fill it issued, so an
+        // MMA warp it frees from a ring hand-off reads landed data and frees slots
+        // that are never refilled.
         const unsigned long long cap = 64ull * limit;
         unsigned long long i = 0;
         for (; i < cap && !*mma_exit; ++i) {
@@ -411,7 +410,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto half_ready = [&](int hh) -> bool {
             if constexpr (G::kWatch) {
                 named_bar_sync(kBarRing0 + static_cast<uint32_t>((f + hh) % G::kSlots), kBarRingThreads);
-                if (*abort_flag) return false;  // released by the abort path: the half may not have landed
             } else {
                 if (hh == 0)
                     for (int k = 0; k < 2; ++k)
