@@ -193,6 +193,15 @@ def test_bwd_invalid_arguments_rejected(lib, over):
     assert call_bwd(**over) == fa.ATTN_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("over", [dict(ws_bytes=1024), dict(q=Q + 8), dict(dq=Q), dict(scale=0.0),
+                                  dict(Hq=3, Hkv=2), dict(dk=K + 256)],
+                         ids=lambda d: ",".join(f"{k}={v}" for k, v in d.items()))
+def test_bwd_head_size_256_validated_like_the_others(lib, over):
+    """The head-size-256 backward (its own kernels) takes the same checks; a bad
+    argument is rejected before anything is launched."""
+    assert call_bwd(D=256, **over) == fa.ATTN_ERR_INVALID_ARG
+
+
 @pytest.mark.parametrize("D", [32, 96, 192])
 def test_bwd_other_head_dims_unsupported(lib, D):
     assert call_bwd(D=D) == fa.ATTN_ERR_UNSUPPORTED
