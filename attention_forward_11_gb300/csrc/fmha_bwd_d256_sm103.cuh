@@ -37,10 +37,13 @@
 //
 // Warps (352 threads): eight elementwise warps (TMEM lane quarter x column half),
 // the MMA warp, the TMA warp (then the release warp of the abort path) and a ring
-// watcher.  The elementwise warps and the watcher hand over to the MMA warp through
-// hardware named barriers, so within an item the MMA warp polls no mbarrier (such
-// a poll would first wait for its queued MMAs to drain), and each half's products
-// start as soon as that half has landed.  Every mbarrier wait is bounded.
+// watcher.  The elementwise warps hand over to the MMA warp through hardware named
+// barriers.  In the dK and dQ launches so does the watcher, for each ring half, so
+// within an item the MMA warp polls no mbarrier (such a poll would first wait for
+// its queued MMAs to drain) and each half's products start as soon as it lands;
+// in the dV launch (deeper ring, usually full ahead) the MMA warp polls both
+// halves of a product once, which measured faster there, and the watcher idles.
+// Every mbarrier wait is bounded.
 #pragma once
 #include <cstdint>
 #include <cuda.h>
