@@ -326,6 +326,16 @@ def test_bwd_d256_shape_sampled():
     _sampled((4, 4096, 4096, 16, 16, 256), 1, seed=91, n_rows=32, kv_pairs=[(0, 3), (3, 12)])
 
 
+def test_bwd_d256_shape_every_element():
+    """B=4, H=16, S=4096, D=256, causal: every element of dq, dk and dv against
+    the oracle's full backward (the kernels given the oracle's O and LSE)."""
+    B, S, H, D = 4, 4096, 16, 256
+    q, k, v, do = problem(B, S, S, H, H, D, seed=93)
+    stats = check(q, k, v, do, 1, 1 / math.sqrt(D), "d256 full shape every element")
+    print("d256 full shape every element, (mean, max excess) in u rms:",
+          {k_: (round(a, 3), round(b, 2)) for k_, (a, b) in stats.items()})
+
+
 def test_bwd_d256_every_element():
     """Head size 256 with every element of dq, dk and dv against the oracle:
     GQA group 2, 2048 rows and keys (16 tiles each way), causal."""
