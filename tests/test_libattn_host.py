@@ -39,7 +39,7 @@ def _declaration(name):
     return m.group(1), params
 
 
-def test_boundary_calls_have_the_surveyed_signatures():
+def test_boundary_calls_have_their_specified_signatures():
     """The three calls of the boundary: the forward, the status string, and the
     device status of the calls made so far (no stream argument)."""
     ret, params = _declaration("attn_fwd")
