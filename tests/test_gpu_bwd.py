@@ -195,10 +195,11 @@ def test_bwd_degenerate_lengths(Sq, Skv, causal, D):
     check(q, k, v, do, causal, scale, f"Sq={Sq} Skv={Skv} causal={causal} D={D}")
 
 
-def test_bwd_many_tiny_batch_entries():
-    q, k, v, do = problem(64, 5, 9, 2, 1, 128, seed=81)
+@pytest.mark.parametrize("D", [128, 256])
+def test_bwd_many_tiny_batch_entries(D):
+    q, k, v, do = problem(64, 5, 9, 2, 1, D, seed=81)
     for causal in (0, 1, 2):
-        check(q, k, v, do, causal, 0.1, f"B=64 causal={causal}")
+        check(q, k, v, do, causal, 0.1, f"B=64 causal={causal} D={D}")
 
 
 @pytest.mark.parametrize("D", [128, 256])
